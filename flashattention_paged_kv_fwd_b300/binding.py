@@ -1,0 +1,243 @@
+"""ctypes binding of libpagedattn.so: argument marshalling only.
+
+Every function takes torch tensors that already live on the GPU, checks that
+their shapes, dtypes and layouts match the C ABI (``include/pagedattn.h``),
+and passes raw device pointers plus the current CUDA stream to the library.
+All arithmetic happens in the library's kernels; there is no fallback path.
+If the shared library is missing the first call raises ``RuntimeError``.
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "PagedAttnError",
+    "library_path",
+    "load_library",
+    "attn_prefill",
+    "kv_append_paged",
+    "attn_decode_paged",
+    "decode_workspace_bytes",
+    "check_err_flag",
+    "new_err_flag",
+    "PA_BF16",
+    "PA_F32",
+]
+
+PA_BF16 = 0
+PA_F32 = 1
+_DTYPES = {torch.bfloat16: PA_BF16, torch.float32: PA_F32}
+DEV_ERRORS = {1: "block id outside the pool", 2: "position beyond the block table",
+              4: "bounded wait gave up"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+class PagedAttnError(RuntimeError):
+    pass
+
+
+def library_path():
+    return os.path.join(_HERE, "lib", "libpagedattn.so")
+
+
+def load_library():
+    """Load (once) and return the ctypes handle of libpagedattn.so."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is not built; run `python -m flashattention_paged_kv_fwd_b300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.pa_status_str.argtypes = [i32]
+    lib.pa_status_str.restype = ctypes.c_char_p
+    lib.pa_attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
+                                    i32, f32, i32, vp, vp]
+    lib.pa_attn_prefill.restype = i32
+    lib.pa_kv_append_paged.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                       i32, i32, vp, vp]
+    lib.pa_kv_append_paged.restype = i32
+    lib.pa_attn_decode_paged.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, i32, i32,
+                                         i32, i32, i32, f32, i32, vp, sz, i32, vp, vp]
+    lib.pa_attn_decode_paged.restype = i32
+    lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.pa_decode_workspace_bytes.restype = sz
+    _LIB = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, what):
+    if status != 0:
+        msg = load_library().pa_status_str(status).decode()
+        raise PagedAttnError(f"{what}: {msg} (status {status})")
+
+
+def _need(cond, msg):
+    if not cond:
+        raise PagedAttnError(msg)
+
+
+def _cuda_contig(name, t, dtype=None):
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+    if dtype is not None:
+        _need(t.dtype == dtype, f"{name} must be {dtype}, got {t.dtype}")
+
+
+def new_err_flag(device=None):
+    """A zeroed int32 device scalar for the kernels' error bits."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_err_flag(err_flag):
+    """Synchronise on the flag and raise if any kernel reported bad data."""
+    v = int(err_flag.item())
+    if v:
+        names = [n for bit, n in DEV_ERRORS.items() if v & bit]
+        raise PagedAttnError(f"device reported: {', '.join(names)} (flags {v})")
+
+
+def attn_prefill(q, k, v, *, causal=True, window=0, scale=None, cu_seqlens=None,
+                 max_seqlen=None, out=None, lse=None, return_lse=True, err_flag=None,
+                 stream=None):
+    """Exact attention of each sequence's queries over its own keys.
+
+    Fixed length: q [B, N, Hq, d], k and v [B, N, Hkv, d].
+    Packed varlen: q [T, Hq, d], k and v [T, Hkv, d] with ``cu_seqlens``
+    (int32 [B+1], on the GPU) and ``max_seqlen``.
+    Returns (o, lse) with o shaped like q and lse float32 [Hq, T].
+    """
+    lib = load_library()
+    _need(q.dtype in _DTYPES, "q must be bfloat16 or float32")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, q.dtype)
+    d = q.shape[-1]
+    hq, hkv = q.shape[-2], k.shape[-2]
+    if cu_seqlens is None:
+        _need(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "q must be [B, N, Hq, d]")
+        B, N = q.shape[0], q.shape[1]
+        _need(k.shape[:2] == (B, N), "k/v must be [B, N, Hkv, d]")
+        T = B * N
+        n_arg, msl = N, N
+    else:
+        _cuda_contig("cu_seqlens", cu_seqlens, torch.int32)
+        _need(q.dim() == 3 and k.dim() == 3 and v.shape == k.shape, "q must be [T, Hq, d]")
+        _need(max_seqlen is not None, "max_seqlen is required with cu_seqlens")
+        B = cu_seqlens.numel() - 1
+        T = q.shape[0]
+        _need(k.shape[0] == T, "k/v must have the same token count as q")
+        n_arg, msl = T, int(max_seqlen)
+    _need(k.shape[-1] == d, "head dims differ")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda_contig("out", out, q.dtype)
+        _need(out.shape == q.shape, "out must match q")
+    if lse is None and return_lse:
+        lse = torch.empty((hq, T), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _cuda_contig("lse", lse, torch.float32)
+        _need(lse.shape == (hq, T), "lse must be [Hq, T]")
+    st = lib.pa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, hq, hkv, n_arg,
+                             d, _ptr(cu_seqlens), msl, 1 if causal else 0, int(window or 0),
+                             float(scale or 0.0), _DTYPES[q.dtype], _ptr(err_flag),
+                             _stream(stream))
+    _check(st, "attn_prefill")
+    return out, lse
+
+
+def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, seq_lens, *, cu_new=None,
+                    err_flag=None, stream=None):
+    """Write new K/V rows into the paged pools in place.
+
+    k_new, v_new [T_new, Hkv, d]; pools [num_blocks, block_size, Hkv, d];
+    block_table int32 [B, max_blocks]; seq_lens int32 [B] (lengths BEFORE
+    the append); cu_new int32 [B+1] or None (one token per sequence).
+    """
+    lib = load_library()
+    _need(k_cache.dtype in _DTYPES, "pools must be bfloat16 or float32")
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache),
+                    ("v_cache", v_cache)):
+        _cuda_contig(name, t, k_cache.dtype)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("seq_lens", seq_lens, torch.int32)
+    num_blocks, block_size, hkv, d = k_cache.shape
+    _need(v_cache.shape == k_cache.shape, "k_cache and v_cache differ in shape")
+    _need(k_new.dim() == 3 and k_new.shape[1:] == (hkv, d) and v_new.shape == k_new.shape,
+          "k_new/v_new must be [T_new, Hkv, d]")
+    B = seq_lens.numel()
+    _need(block_table.dim() == 2 and block_table.shape[0] == B, "block_table must be [B, max_blocks]")
+    if cu_new is not None:
+        _cuda_contig("cu_new", cu_new, torch.int32)
+        _need(cu_new.numel() == B + 1, "cu_new must have B+1 entries")
+    st = lib.pa_kv_append_paged(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                _ptr(cu_new), k_new.shape[0], B, hkv, d, block_size, num_blocks,
+                                _DTYPES[k_cache.dtype], _ptr(err_flag), _stream(stream))
+    _check(st, "kv_append_paged")
+
+
+def decode_workspace_bytes(batch, num_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                           block_size=16, window=0, num_splits=0):
+    return int(load_library().pa_decode_workspace_bytes(batch, num_heads, num_kv_heads, head_dim,
+                                                        max_blocks_per_seq, block_size,
+                                                        int(window or 0), num_splits))
+
+
+def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, *, window=0, scale=None,
+                      num_splits=0, out=None, lse=None, return_lse=True, workspace=None,
+                      err_flag=None, stream=None):
+    """One query per sequence over its paged cache.
+
+    q [B, Hq, d]; pools [num_blocks, 16, Hkv, d]; block_table int32
+    [B, max_blocks]; seq_lens int32 [B] = keys visible (current token
+    included). Returns (o [B, Hq, d], lse float32 [Hq, B]).
+    """
+    lib = load_library()
+    _need(q.dtype in _DTYPES, "q must be bfloat16 or float32")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda_contig(name, t, q.dtype)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("seq_lens", seq_lens, torch.int32)
+    B, hq, d = q.shape
+    num_blocks, block_size, hkv, dk = k_cache.shape
+    _need(dk == d and v_cache.shape == k_cache.shape, "pool shapes do not match q")
+    _need(block_table.dim() == 2 and block_table.shape[0] == B, "block_table must be [B, max_blocks]")
+    _need(seq_lens.numel() == B, "seq_lens must have B entries")
+    max_blocks = block_table.shape[1]
+    need = decode_workspace_bytes(B, hq, hkv, d, max_blocks, block_size, window, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, B), dtype=torch.float32, device=q.device)
+    st = lib.pa_attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                  max_blocks, _ptr(seq_lens), _ptr(out), _ptr(lse), B, hq, hkv, d,
+                                  block_size, num_blocks, int(window or 0), float(scale or 0.0),
+                                  int(num_splits), _ptr(workspace),
+                                  0 if workspace is None else workspace.numel(),
+                                  _DTYPES[q.dtype], _ptr(err_flag), _stream(stream))
+    _check(st, "attn_decode_paged")
+    return out, lse
+
+
+def default_scale(head_dim):
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,111 @@
+// kv_append_paged: scatter new tokens' K/V rows into the paged pools.
+//
+// "Module 09: Efficient Attention", section "Code: A Paged KV Cache from
+// Scratch": the token at logical position t of a sequence is stored at
+// (block_table[t // block_size], t % block_size) of a pool shaped
+// (num_blocks, block_size, num_kv_heads, head_dim). One token's row for all
+// KV heads is contiguous both in the input ([T_new, Hkv, d]) and in the pool,
+// so each token is one contiguous copy of Hkv*d*elem bytes, moved as 16-byte
+// vectors by one warp. Bit-exact by construction (no arithmetic on values).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pa_ptx.cuh"
+#include "pa_kernels.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kAppendWarps = 8;       // tokens per CTA
+constexpr int kMaxCuInSmem = 4096;    // sequences whose offsets are staged in smem
+constexpr int kUnroll = 4;            // 16-byte vectors in flight per lane per tensor
+
+__device__ __forceinline__ int find_sequence(const int32_t* cu, int n_seq, int t) {
+  // largest b with cu[b] <= t (cu is non-decreasing; empty sequences skipped)
+  int lo = 0, hi = n_seq - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kAppendWarps * 32)
+kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                 uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                 const int32_t* __restrict__ table, int max_blocks,
+                 const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_new,
+                 int n_seq, int n_tok, int row_vecs, int block_size, int num_blocks,
+                 int32_t* err) {
+  __shared__ int32_t cu_s[kMaxCuInSmem + 1];
+  const bool staged = cu_new != nullptr && n_seq <= kMaxCuInSmem;
+  if (staged) {
+    for (int i = threadIdx.x; i <= n_seq; i += blockDim.x) cu_s[i] = cu_new[i];
+    __syncthreads();
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kAppendWarps + warp;
+  if (t >= n_tok) return;
+
+  int b, first;
+  if (cu_new == nullptr) {
+    b = t;
+    first = t;
+  } else if (staged) {
+    b = find_sequence(cu_s, n_seq, t);
+    first = cu_s[b];
+  } else {
+    b = find_sequence(cu_new, n_seq, t);
+    first = cu_new[b];
+  }
+  const int pos = seq_lens[b] + (t - first);
+  const int lblk = pos / block_size;
+  if (pos < 0 || lblk >= max_blocks) {
+    if (lane == 0) raise_err(err, kDevErrBadPosition);
+    return;
+  }
+  const int blk = table[static_cast<int64_t>(b) * max_blocks + lblk];
+  if (blk < 0 || blk >= num_blocks) {
+    if (lane == 0) raise_err(err, kDevErrBadBlock);
+    return;
+  }
+  const int64_t src = static_cast<int64_t>(t) * row_vecs;
+  const int64_t dst = (static_cast<int64_t>(blk) * block_size + pos % block_size) * row_vecs;
+  for (int i0 = 0; i0 < row_vecs; i0 += 32 * kUnroll) {
+    uint4 kv[kUnroll], vv[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u * 32 + lane;
+      if (i < row_vecs) {
+        kv[u] = __ldg(k_new + src + i);
+        vv[u] = __ldg(v_new + src + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u * 32 + lane;
+      if (i < row_vecs) {
+        k_cache[dst + i] = kv[u];
+        v_cache[dst + i] = vv[u];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const int32_t* table, int max_blocks, const int32_t* seq_lens,
+                             const int32_t* cu_new, int n_tok, int n_seq, int row_bytes,
+                             int block_size, int num_blocks, int32_t* err, cudaStream_t s) {
+  if (n_tok == 0) return cudaSuccess;
+  const int grid = (n_tok + kAppendWarps - 1) / kAppendWarps;
+  kv_append_kernel<<<grid, kAppendWarps * 32, 0, s>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), table, max_blocks, seq_lens,
+      cu_new, n_seq, n_tok, row_bytes / 16, block_size, num_blocks, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

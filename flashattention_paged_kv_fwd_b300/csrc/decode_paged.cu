@@ -1,0 +1,551 @@
+// attn_decode_paged: one query per sequence over its paged KV cache, with
+// split-KV ranges merged through their log-sum-exp.
+//
+// Sources: the decode step ("Генерация и KV-кэш", section "KV-кэш для одной
+// головы на NumPy": the new token's query against every cached key, stable
+// softmax), the gather through the block table ("Module 09: Efficient
+// Attention", section "The Block Table"), the query-to-KV-head mapping (same
+// notebook, section "The Math: Sharing Keys and Values"), and the online
+// recurrence with rescaling by e^{m_old - m_new} ("Ли Хунъи ... 2026", lecture
+// "Ускоряем генерацию, часть 1: FlashAttention"). Merging two ranges is the
+// same recurrence applied to their (max, sum) pairs, written with
+// lse = m + ln(l).
+//
+// bf16 design (memory-bound, ~1-8 FLOP per byte read):
+//  * CTA = (sequence, group of `hg` KV heads, range of `chunk` blocks).
+//  * One producer thread walks the range's slice of the block table (staged
+//    in shared memory) and issues TMA copies of each block's K and V rows for
+//    the CTA's heads into a ring of `stages` shared-memory buffers. Each copy
+//    is one (head, 64-element panel) box of 16 tokens x 128 B, 128-byte
+//    swizzled so that the ldmatrix reads below are bank-conflict free.
+//  * One consumer warp per (KV head, 16 query heads): the G = Hq/Hkv query
+//    heads that share the KV head are packed as the 16 rows of an m16n8k16
+//    warp MMA (rows past G are zero), so K and V are read from shared memory
+//    once per group. S = Q K^T and O += P V run on the tensor cores with fp32
+//    accumulators; the running (max, sum) lives in registers and is reduced
+//    across the 4 threads that share a row with warp shuffles.
+//  * Scores of tokens outside [first visible, seq_len) are set to -inf and
+//    their V rows zeroed, so unused slots of a block may hold anything.
+#include <cmath>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "pa_kernels.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kBlk = 16;              // tokens per block (page)
+constexpr int kBox = kBlk * 128;      // bytes of one (head, panel) box
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kNegInf = -INFINITY;
+
+struct SeqRange {
+  int len;      // visible keys end (exclusive), clamped to the table
+  int t_begin;  // first visible key
+  int p_begin;  // first block touched
+  int n_pages;  // blocks touched
+  int n_split;  // ranges
+};
+
+__device__ __forceinline__ SeqRange seq_range(int len, int max_blocks, int window, int chunk,
+                                              int32_t* err, bool report) {
+  SeqRange r;
+  if (len < 0 || len > max_blocks * kBlk) {
+    if (report) raise_err(err, kDevErrBadPosition);
+    len = len < 0 ? 0 : max_blocks * kBlk;
+  }
+  r.len = len;
+  r.t_begin = (window > 0 && len > window) ? len - window : 0;
+  r.p_begin = r.t_begin / kBlk;
+  r.n_pages = len > 0 ? (len + kBlk - 1) / kBlk - r.p_begin : 0;
+  r.n_split = (r.n_pages + chunk - 1) / chunk;
+  return r;
+}
+
+// ---------------------------------------------------------------- bf16 path
+// Consumer warps per CTA at most (plus one producer warp), chosen so the
+// accumulators (d/8 x 4 fp32) and Q fragments stay in registers.
+template <int D>
+constexpr int kMaxConsumerWarps = D == 128 ? 8 : 12;
+
+template <int D>
+__global__ void __launch_bounds__((kMaxConsumerWarps<D> + 1) * 32, 1)
+decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const DecodeArgs a, const int chunk,
+                   const int num_splits, const int hg, const int mt, const int ns) {
+  constexpr int P = D / 64;  // 128-byte panels per token row
+  const int G = a.Hq / a.Hkv;
+  const int b = blockIdx.z, hc = blockIdx.y, s = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = hg * mt;  // consumer warps
+
+  const SeqRange r = seq_range(a.seq_lens[b], a.max_blocks, a.window, chunk, a.err,
+                               s == 0 && hc == 0 && threadIdx.x == 0);
+  if (s >= (r.n_split > 0 ? r.n_split : 1)) return;
+
+  if (r.n_pages == 0) {  // no visible key: o = 0, lse = -inf
+    const int h0 = hc * hg * G, nh = hg * G;
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.o);
+    for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
+      o[(static_cast<int64_t>(b) * a.Hq + h0) * D + i] = __float2bfloat16_rn(0.f);
+    if (a.lse)
+      for (int i = threadIdx.x; i < nh; i += blockDim.x) a.lse[(h0 + i) * a.B + b] = kNegInf;
+    return;
+  }
+  const int pstart = r.p_begin + s * chunk;
+  const int npg = min(chunk, r.n_pages - s * chunk);
+  const bool single = r.n_split == 1;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t stage_bytes = 2u * hg * P * kBox;
+  const uint32_t bars = base + ns * stage_bytes;  // full[ns], empty[ns]
+  int32_t* phys_s = reinterpret_cast<int32_t*>(gbase + ns * stage_bytes + 16 * ns);
+  int32_t* tab_s = phys_s + ns;
+  volatile int32_t* abort_s = tab_s + chunk;
+  auto full = [&](int i) { return bars + 8u * i; };
+  auto empty = [&](int i) { return bars + 8u * (ns + i); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), nw);
+    }
+    *abort_s = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < npg; i += blockDim.x)
+    tab_s[i] = a.table[static_cast<int64_t>(b) * a.max_blocks + pstart + i];
+  __syncthreads();
+
+  if (warp == nw) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+      int issued = 0;
+      uint32_t valid_mask = 0;  // validity of the last `ns` issued blocks (bit per stage)
+      for (int i = 0; i < npg; ++i) {
+        const int st = i % ns, u = i / ns;
+        if (u > 0 && !mbar_wait(empty(st), (u - 1) & 1)) {
+          raise_err(a.err, kDevErrTimeout);
+          *abort_s = 1;
+          break;
+        }
+        if (*abort_s) break;
+        const int phys = tab_s[i];
+        const bool ok = phys >= 0 && phys < a.num_blocks;
+        if (!ok) raise_err(a.err, kDevErrBadBlock);
+        phys_s[st] = ok ? phys : -1;
+        if (ok) {
+          mbar_arrive_expect_tx(full(st), stage_bytes);
+          const uint32_t sb = base + st * stage_bytes;
+          for (int g = 0; g < hg; ++g) {
+            const int head = hc * hg + g;
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+              tma_load_4d(sb + (g * P + p) * kBox, &kmap, full(st), p * 64, head, 0, phys);
+              tma_load_4d(sb + ((hg + g) * P + p) * kBox, &vmap, full(st), p * 64, head, 0, phys);
+            }
+          }
+          valid_mask |= 1u << st;
+        } else {
+          valid_mask &= ~(1u << st);
+          mbar_arrive(full(st));
+        }
+        issued = i + 1;
+      }
+      // Let no copy land after the CTA exits: wait for the last use of each
+      // stage (already complete unless the loop was abandoned).
+      for (int i = issued - ns > 0 ? issued - ns : 0; i < issued; ++i) {
+        const int st = i % ns;
+        if (valid_mask & (1u << st)) mbar_wait(full(st), (i / ns) & 1, 100000000ull);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = warp / mt, mti = warp % mt;
+  const int kvh = hc * hg + g;
+  const int qh0 = kvh * G + mti * 16;
+  const int nrows = min(16, G - mti * 16);
+  const int gr = lane >> 2, tq = lane & 3;
+  const float sl2 = a.scale_log2;
+
+  uint32_t qa[D / 16][4];
+  {
+    const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
+    const int64_t ra = (static_cast<int64_t>(b) * a.Hq + qh0 + gr) * (D / 2);
+    const int64_t rb = ra + 8 * (D / 2);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = gr < nrows ? q32[ra + kk * 8 + tq] : 0u;
+      qa[kk][1] = gr + 8 < nrows ? q32[rb + kk * 8 + tq] : 0u;
+      qa[kk][2] = gr < nrows ? q32[ra + kk * 8 + 4 + tq] : 0u;
+      qa[kk][3] = gr + 8 < nrows ? q32[rb + kk * 8 + 4 + tq] : 0u;
+    }
+  }
+
+  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+  float acc[D / 8][4];
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+  const int mi = lane >> 3, rr = lane & 7;
+  const int ktok = ((mi >> 1) << 3) + rr;  // token row this lane addresses for K
+  const int vtok = ((mi & 1) << 3) + rr;   // ... and for V (transposed load)
+
+  for (int i = 0; i < npg; ++i) {
+    const int st = i % ns;
+    if (!mbar_wait(full(st), (i / ns) & 1)) {
+      raise_err(a.err, kDevErrTimeout);
+      *abort_s = 1;
+      break;
+    }
+    const int phys = phys_s[st];
+    if (phys >= 0) {
+      const uint32_t kb = base + st * stage_bytes + g * P * kBox;
+      const uint32_t vb = base + st * stage_bytes + (hg + g) * P * kBox;
+      const int tok0 = (pstart + i) * kBlk;
+
+      float sc[2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int c = kk * 2 + (mi & 1);
+        const uint32_t addr = kb + (c >> 3) * kBox + ktok * 128 + (((c & 7) ^ (ktok & 7)) << 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(addr, b0, b1, b2, b3);
+        mma_bf16_16816(sc[0], qa[kk], b0, b1);
+        mma_bf16_16816(sc[1], qa[kk], b2, b3);
+      }
+
+      const bool edge = (tok0 + kBlk > r.len) || (tok0 < r.t_begin);
+      uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+      if (edge) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = tok0 + 8 * t + 2 * tq + (e & 1);
+            if (tok >= r.len || tok < r.t_begin) sc[t][e] = kNegInf;
+          }
+        auto ok = [&](int tok) { return tok < r.len && tok >= r.t_begin; };
+        const int ta = tok0 + 2 * tq, tb = tok0 + 8 + 2 * tq;
+        mlo = (ok(ta) ? 0x0000FFFFu : 0u) | (ok(ta + 1) ? 0xFFFF0000u : 0u);
+        mhi = (ok(tb) ? 0x0000FFFFu : 0u) | (ok(tb + 1) ? 0xFFFF0000u : 0u);
+      }
+
+      // online softmax (log2 domain), rows gr (e = 0,1) and gr + 8 (e = 2,3)
+      float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) * sl2;
+      float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])) * sl2;
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float mu0 = mn0 == kNegInf ? 0.f : mn0;
+      const float mu1 = mn1 == kNegInf ? 0.f : mn1;
+      const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+      m0 = mn0;
+      m1 = mn1;
+      float ps[2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        ps[t][0] = ex2(fmaf(sc[t][0], sl2, -mu0));
+        ps[t][1] = ex2(fmaf(sc[t][1], sl2, -mu0));
+        ps[t][2] = ex2(fmaf(sc[t][2], sl2, -mu1));
+        ps[t][3] = ex2(fmaf(sc[t][3], sl2, -mu1));
+      }
+      l0 = l0 * al0 + (ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1]);
+      l1 = l1 * al1 + (ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3]);
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) {
+        acc[j][0] *= al0;
+        acc[j][1] *= al0;
+        acc[j][2] *= al1;
+        acc[j][3] *= al1;
+      }
+      const uint32_t pa[4] = {pack_bf16(ps[0][0], ps[0][1]), pack_bf16(ps[0][2], ps[0][3]),
+                              pack_bf16(ps[1][0], ps[1][1]), pack_bf16(ps[1][2], ps[1][3])};
+#pragma unroll
+      for (int jj = 0; jj < D / 16; ++jj) {
+        const int c = jj * 2 + (mi >> 1);
+        const uint32_t addr = vb + (c >> 3) * kBox + vtok * 128 + (((c & 7) ^ (vtok & 7)) << 4);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(addr, v0, v1, v2, v3);
+        mma_bf16_16816(acc[2 * jj], pa, v0 & mlo, v1 & mhi);
+        mma_bf16_16816(acc[2 * jj + 1], pa, v2 & mlo, v3 & mhi);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(st));
+  }
+
+  // ------------------------------------------------------------- epilogue
+  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int row = gr + 8 * half;
+    if (row >= nrows) continue;
+    const int h = qh0 + row;
+    const float l = half ? l1 : l0;
+    const float m = half ? m1 : m0;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
+    const int64_t bh = static_cast<int64_t>(b) * a.Hq + h;
+    if (single) {
+      uint32_t* o32 = static_cast<uint32_t*>(a.o) + bh * (D / 2);
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j)
+        o32[j * 4 + tq] = pack_bf16(acc[j][2 * half] * inv, acc[j][2 * half + 1] * inv);
+      if (tq == 0 && a.lse) a.lse[h * a.B + b] = lse_v;
+    } else {
+      float2* w = reinterpret_cast<float2*>(a.ws_o + (bh * num_splits + s) * D);
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j)
+        w[j * 4 + tq] = make_float2(acc[j][2 * half] * inv, acc[j][2 * half + 1] * inv);
+      if (tq == 0) a.ws_lse[bh * num_splits + s] = lse_v;
+    }
+  }
+}
+
+// --------------------------------------------------------------- fp32 path
+// CUDA-core reference-speed path for fp32 caches: one warp per (sequence,
+// query head, range); each lane owns d/32 columns; dot products are reduced
+// with warp shuffles.
+template <int D>
+__global__ void __launch_bounds__(128)
+decode_f32_kernel(const DecodeArgs a, const int chunk, const int num_splits) {
+  const int b = blockIdx.z, s = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 4 + warp;
+  if (h >= a.Hq) return;
+  const int G = a.Hq / a.Hkv, g = h / G;
+  const SeqRange r = seq_range(a.seq_lens[b], a.max_blocks, a.window, chunk, a.err,
+                               s == 0 && h == 0 && lane == 0);
+  if (s >= (r.n_split > 0 ? r.n_split : 1)) return;
+  const int64_t bh = static_cast<int64_t>(b) * a.Hq + h;
+  float* o = static_cast<float*>(a.o);
+  if (r.n_pages == 0) {
+    for (int c = lane; c < D; c += 32) o[bh * D + c] = 0.f;
+    if (lane == 0 && a.lse) a.lse[h * a.B + b] = kNegInf;
+    return;
+  }
+  const float* qf = static_cast<const float*>(a.q) + bh * D;
+  const float* kc = static_cast<const float*>(a.k_cache);
+  const float* vc = static_cast<const float*>(a.v_cache);
+  float qv[D / 32], acc[D / 32];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) {
+    qv[i] = qf[lane + 32 * i];
+    acc[i] = 0.f;
+  }
+  float m = kNegInf, l = 0.f;
+  const int pstart = r.p_begin + s * chunk;
+  const int npg = min(chunk, r.n_pages - s * chunk);
+  for (int i = 0; i < npg; ++i) {
+    const int page = pstart + i;
+    const int phys = a.table[static_cast<int64_t>(b) * a.max_blocks + page];
+    if (phys < 0 || phys >= a.num_blocks) {
+      if (lane == 0) raise_err(a.err, kDevErrBadBlock);
+      continue;
+    }
+    for (int t = 0; t < kBlk; ++t) {
+      const int tok = page * kBlk + t;
+      if (tok < r.t_begin || tok >= r.len) continue;
+      const int64_t row = ((static_cast<int64_t>(phys) * kBlk + t) * a.Hkv + g) * D;
+      float dot = 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) dot = fmaf(qv[c], kc[row + lane + 32 * c], dot);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, off);
+      const float s2 = dot * a.scale_log2;
+      const float mn = fmaxf(m, s2);
+      const float al = ex2(m - mn);
+      const float p = ex2(s2 - mn);
+      l = l * al + p;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(p, vc[row + lane + 32 * c], acc[c] * al);
+      m = mn;
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
+  if (r.n_split == 1) {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) o[bh * D + lane + 32 * c] = acc[c] * inv;
+    if (lane == 0 && a.lse) a.lse[h * a.B + b] = lse_v;
+  } else {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) a.ws_o[(bh * num_splits + s) * D + lane + 32 * c] = acc[c] * inv;
+    if (lane == 0) a.ws_lse[bh * num_splits + s] = lse_v;
+  }
+}
+
+// ------------------------------------------------------------------ merge
+// lse = ln sum_s e^{lse_s}; o = sum_s e^{lse_s - lse} o_s. One warp per
+// (sequence, query head); sequences that used a single range were finished
+// by the decode kernel and are skipped here.
+template <typename OutT, int D>
+__global__ void __launch_bounds__(256)
+decode_merge_kernel(const DecodeArgs a, const int chunk, const int num_splits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int idx = blockIdx.x * 8 + warp;
+  if (idx >= a.B * a.Hq) return;
+  const int b = idx / a.Hq, h = idx % a.Hq;
+  const SeqRange r = seq_range(a.seq_lens[b], a.max_blocks, a.window, chunk, a.err, false);
+  if (r.n_split <= 1) return;
+  const float* ls = a.ws_lse + static_cast<int64_t>(idx) * num_splits;
+  float mx = kNegInf;
+  for (int i = lane; i < r.n_split; i += 32) mx = fmaxf(mx, ls[i]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+  float acc[D / 32];
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) acc[c] = 0.f;
+  float total = 0.f;
+  const float* wo = a.ws_o + static_cast<int64_t>(idx) * num_splits * D;
+  for (int i = 0; i < r.n_split; ++i) {
+    const float w = expf(ls[i] - mx);
+    total += w;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(w, wo[i * D + lane + 32 * c], acc[c]);
+  }
+  const float inv = 1.f / total;
+  OutT* o = static_cast<OutT*>(a.o) + static_cast<int64_t>(idx) * D;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    if constexpr (sizeof(OutT) == 2)
+      o[lane + 32 * c] = __float2bfloat16_rn(acc[c] * inv);
+    else
+      o[lane + 32 * c] = acc[c] * inv;
+  }
+  if (lane == 0 && a.lse) a.lse[h * a.B + b] = mx + logf(total);
+}
+
+int g_attr_done[2][64];
+
+template <int D>
+void ensure_smem_attr(size_t bytes) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (g_attr_done[D == 128][dev] < static_cast<int>(bytes)) {
+    cudaFuncSetAttribute(decode_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(bytes));
+    g_attr_done[D == 128][dev] = static_cast<int>(bytes);
+  }
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_size, int window,
+                       int num_splits_req, int sm_count, bool f32) {
+  DecodePlan p{};
+  const int G = Hq / Hkv;
+  int eff = max_blocks;  // blocks one sequence can touch
+  if (window > 0) {
+    const int wb = (window + block_size - 2) / block_size + 1;
+    eff = wb < max_blocks ? wb : max_blocks;
+  }
+  if (eff < 1) eff = 1;
+  if (f32) {
+    p.hg = 1;
+    p.head_chunks = 1;
+    p.mt = 1;
+    p.stages = 0;
+    p.threads = 128;
+  } else {
+    const int P = d / 64;
+    const int max_warps = d == 128 ? kMaxConsumerWarps<128> : kMaxConsumerWarps<64>;
+    p.mt = (G + 15) / 16;
+    int hg = 1;
+    for (int c = 1; c <= Hkv; ++c)
+      if (Hkv % c == 0 && c * p.mt <= max_warps && 2 * c * P * kBox <= 64 * 1024) hg = c;
+    p.hg = hg;
+    p.head_chunks = Hkv / hg;
+    const int stage = 2 * hg * P * kBox;
+    int ns = (200 * 1024) / stage;
+    p.stages = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+    p.threads = (hg * p.mt + 1) * 32;
+  }
+  int chunk;
+  if (num_splits_req > 0) {
+    chunk = (eff + num_splits_req - 1) / num_splits_req;
+  } else {
+    const long long units = static_cast<long long>(B) * p.head_chunks;
+    const long long target = 2LL * (sm_count > 0 ? sm_count : 148);
+    long long c = (units * eff + target - 1) / target;
+    c = c < 4 ? 4 : (c > 64 ? 64 : c);
+    chunk = static_cast<int>(c);
+  }
+  if (chunk > eff) chunk = eff;
+  if (chunk < 1) chunk = 1;
+  p.chunk = chunk;
+  p.num_splits = (eff + chunk - 1) / chunk;
+  if (!f32) {
+    const int P = d / 64;
+    const size_t stage = 2ull * p.hg * P * kBox;
+    p.smem = 1024 + p.stages * stage + 16ull * p.stages + 4ull * p.stages + 4ull * chunk + 16;
+  }
+  if (p.num_splits > 1) {
+    const size_t n = static_cast<size_t>(B) * Hq * p.num_splits;
+    const size_t o_bytes = (n * d * 4 + 255) / 256 * 256;
+    p.workspace = o_bytes + (n * 4 + 255) / 256 * 256;
+  } else {
+    p.workspace = 0;
+  }
+  return p;
+}
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodePlan& p, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t s) {
+  const dim3 grid(p.num_splits, p.head_chunks, a.B);
+  if (a.d == 128) {
+    ensure_smem_attr<128>(p.smem);
+    decode_bf16_kernel<128><<<grid, p.threads, p.smem, s>>>(kmap, vmap, a, p.chunk, p.num_splits,
+                                                            p.hg, p.mt, p.stages);
+  } else {
+    ensure_smem_attr<64>(p.smem);
+    decode_bf16_kernel<64><<<grid, p.threads, p.smem, s>>>(kmap, vmap, a, p.chunk, p.num_splits,
+                                                           p.hg, p.mt, p.stages);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.num_splits <= 1) return e;
+  const int mblocks = (a.B * a.Hq + 7) / 8;
+  if (a.d == 128)
+    decode_merge_kernel<__nv_bfloat16, 128><<<mblocks, 256, 0, s>>>(a, p.chunk, p.num_splits);
+  else
+    decode_merge_kernel<__nv_bfloat16, 64><<<mblocks, 256, 0, s>>>(a, p.chunk, p.num_splits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_f32(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s) {
+  const dim3 grid(p.num_splits, (a.Hq + 3) / 4, a.B);
+  if (a.d == 128)
+    decode_f32_kernel<128><<<grid, 128, 0, s>>>(a, p.chunk, p.num_splits);
+  else
+    decode_f32_kernel<64><<<grid, 128, 0, s>>>(a, p.chunk, p.num_splits);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.num_splits <= 1) return e;
+  const int mblocks = (a.B * a.Hq + 7) / 8;
+  if (a.d == 128)
+    decode_merge_kernel<float, 128><<<mblocks, 256, 0, s>>>(a, p.chunk, p.num_splits);
+  else
+    decode_merge_kernel<float, 64><<<mblocks, 256, 0, s>>>(a, p.chunk, p.num_splits);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,77 @@
+// Internal launcher interface between the C ABI (capi.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// ------------------------------------------------------------------ append
+cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const int32_t* table, int max_blocks, const int32_t* seq_lens,
+                             const int32_t* cu_new, int n_tok, int n_seq, int row_bytes,
+                             int block_size, int num_blocks, int32_t* err, cudaStream_t s);
+
+// ------------------------------------------------------------------ decode
+// How one decode call is cut into CTAs. Each sequence's visible blocks
+// [first, last] are cut into ranges of `chunk` blocks; range s of sequence b
+// is one CTA (for each group of `hg` KV heads). Sequences with more than one
+// range write normalised partials (o_s, lse_s) to the workspace and a merge
+// kernel combines them.
+struct DecodePlan {
+  int chunk;       // blocks per range
+  int num_splits;  // ranges per sequence at most (grid.x)
+  int hg;          // KV heads per CTA
+  int head_chunks; // Hkv / hg (grid.y)
+  int mt;          // 16-row MMA tiles per KV head (ceil(G / 16))
+  int stages;      // pipeline depth (pages in flight per CTA)
+  int threads;
+  size_t smem;
+  size_t workspace;  // bytes of partial outputs, 0 when num_splits == 1
+};
+
+DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_size, int window,
+                       int num_splits_req, int sm_count, bool f32);
+
+struct DecodeArgs {
+  const void* q;
+  void* o;
+  float* lse;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* table;
+  const int32_t* seq_lens;
+  float* ws_o;    // [B, Hq, num_splits, d]
+  float* ws_lse;  // [B, Hq, num_splits]
+  int32_t* err;
+  int max_blocks, num_blocks, B, Hq, Hkv, d, window;
+  float scale_log2;
+};
+
+cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodePlan& p, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t s);
+cudaError_t launch_decode_f32(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s);
+
+// ----------------------------------------------------------------- prefill
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const int32_t* cu_seqlens;  // nullptr => fixed length N
+  int32_t* err;
+  int B, Hq, Hkv, N, T, d, max_seqlen, causal, window;
+  float scale_log2;
+};
+
+cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& qmap,
+                                const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                cudaStream_t s);
+cudaError_t launch_prefill_f32(const PrefillArgs& a, cudaStream_t s);
+
+size_t prefill_bf16_smem(int d);
+
+}  // namespace pa

@@ -1,0 +1,182 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn.so: exact scaled-dot-product attention
+ * computed FlashAttention-style on one B300 (sm_103a), over contiguous
+ * (prefill) and paged (decode) key/value storage.
+ *
+ * The operation. For query row i of a sequence with Lq queries and Lk keys,
+ * and query head h:
+ *
+ *   o[i,h,:] = sum_j softmax_j( scale * q[i,h,:] . k[j,g,:] ) v[j,g,:]
+ *   lse[h,i] = ln sum_j exp( scale * q[i,h,:] . k[j,g,:] )
+ *
+ * over the visible keys j, with g = floor(h / (Hq / Hkv)) and scale defaulting
+ * to 1/sqrt(d). Sources: "Module 09: Efficient Attention" (learnllm notebook),
+ * section "The Math: Sharing Keys and Values" (the formula, n_rep and the
+ * query-to-KV-head mapping; MHA, GQA and MQA are Hkv = Hq, 1 < Hkv < Hq and
+ * Hkv = 1). The score matrix is never written to memory: keys are streamed in
+ * tiles with a running (max, sum) that is rescaled whenever the max grows
+ * ("Cache KV, atención flash y optimización de la inferencia", section "La
+ * atención de flash el truco de la balsa"; "Ли Хунъи, «Машинное обучение»
+ * 2026 ...", lecture "Ускоряем генерацию, часть 1: FlashAttention").
+ *
+ * Visibility. Query row i sits at absolute position p_i = Lk - Lq + i (the
+ * causal mask is aligned to the bottom-right corner: "Генерация и KV-кэш",
+ * section "Три ловушки, на которых спотыкаются все", trap 2). Causal: j <= p_i.
+ * Sliding window W > 0 (causal only): additionally j > p_i - W, so the
+ * diagonal counts toward W ("Module 09: Efficient Attention", section
+ * "Attention Mask Gallery", sliding_window_mask(6, window=3)).
+ *
+ * LSE is the natural logarithm of the softmax denominator (not given on the
+ * pages; see the design notes). A query with no visible key gets o = 0 and
+ * lse = -inf.
+ *
+ * Conventions shared by every call:
+ *  - All pointers are DEVICE pointers except where stated; all tensors are
+ *    dense and row-major in the index order given; the caller owns every
+ *    buffer. The library never allocates device memory and keeps no state
+ *    between calls (it caches one driver entry point and the SM count).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy stream).
+ *  - Return value: PA_OK, or a host-detected error (nothing is launched).
+ *  - err_flag (optional, may be NULL): an int32 in device memory that kernels
+ *    OR PA_DEV_* bits into when they meet bad data (a block id outside the
+ *    pool, a position beyond a block table, a bounded wait that gave up).
+ *    Outputs are undefined where a bit was raised. Kernels never trap; the
+ *    caller reads the flag after synchronising. The library never clears it.
+ *  - dtype PA_BF16: bf16 inputs and outputs, fp32 accumulation. PA_F32: fp32
+ *    inputs and outputs (a CUDA-core correctness path), fp32 accumulation.
+ *  - Head dimension d must be 64 or 128.
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_BF16 = 0, PA_F32 = 1 } pa_dtype;
+
+enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, Hkv not dividing Hq */
+  PA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. window without causal) */
+  PA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, encode) */
+  PA_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
+};
+
+enum { PA_DEV_BAD_BLOCK = 1, PA_DEV_BAD_POSITION = 2, PA_DEV_TIMEOUT = 4 };
+
+/* Short description of a status code (static string). */
+PA_API const char* pa_status_str(int status);
+
+/*
+ * attn_prefill -- causal / sliding-window / full attention of each sequence's
+ * queries over its own keys (Lq = Lk per sequence), GQA through Hkv.
+ * "Cache KV, atención flash ...", section "La atención de flash el truco de la
+ * balsa" (tile loop over K/V with the output written once per query tile);
+ * "Генерация и KV-кэш", section "Две фазы генерации: prefill и decode".
+ *
+ *  q    [T, Hq, d]   queries, token-major (T = total tokens of the batch)
+ *  k, v [T, Hkv, d]  keys / values, token-major
+ *  o    [T, Hq, d]   output (same dtype as q); must not alias q, k or v
+ *  lse  [Hq, T]      float32 natural-log LSE per (head, token); may be NULL
+ *  B    number of sequences
+ *  N    tokens per sequence when cu_seqlens is NULL (then T = B*N); when
+ *       cu_seqlens is given, N is the total packed token count T
+ *  cu_seqlens  NULL, or int32[B+1] device array of packed sequence offsets
+ *       (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[B] = T); zero-length
+ *       sequences are allowed
+ *  max_seqlen  with cu_seqlens: an upper bound on every sequence's length
+ *  causal      1 = causal, 0 = every query sees every key of its sequence
+ *  window      <= 0: none; > 0: sliding window W (requires causal)
+ *  scale       <= 0: 1/sqrt(d)
+ * Alignment: q, k, v, o 16-byte aligned; lse 4-byte aligned.
+ */
+PA_API int pa_attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int Hq, int Hkv, int N, int d, const int32_t* cu_seqlens, int max_seqlen,
+                    int causal, int window, float scale, pa_dtype dtype, int32_t* err_flag,
+                    void* stream);
+
+/*
+ * kv_append_paged -- write new tokens' keys and values into the paged pools.
+ * "Module 09: Efficient Attention", section "Code: A Paged KV Cache from
+ * Scratch": token t of a sequence lives at (block_table[t / block_size],
+ * t % block_size) of a pool shaped (num_blocks, block_size, Hkv, d).
+ * A pure copy: the pools receive the new rows bit for bit.
+ *
+ *  k_new, v_new  [T_new, Hkv, d]  rows to append, token-major
+ *  k_cache, v_cache [num_blocks, block_size, Hkv, d]  pools, written in place
+ *  block_table   int32 [B, max_blocks_per_seq]; entries past a sequence's
+ *                last block are never read (any value)
+ *  seq_lens      int32 [B]: tokens each sequence holds BEFORE this append;
+ *                the library never modifies it (the caller advances it)
+ *  cu_new        NULL (one new token per sequence, T_new = B) or int32[B+1]
+ *                offsets of each sequence's new rows in k_new / v_new
+ *  num_new_tokens  T_new (must equal cu_new[B] when cu_new is given)
+ * The blocks a write lands in must already be claimed by the caller's
+ * allocator; an entry outside [0, num_blocks) or a position beyond the table
+ * raises a PA_DEV_* bit and that row is skipped.
+ * Alignment: every pointer 16-byte aligned; Hkv*d*elem_size a multiple of 16.
+ */
+PA_API int pa_kv_append_paged(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                       const int32_t* block_table, int max_blocks_per_seq,
+                       const int32_t* seq_lens, const int32_t* cu_new, int num_new_tokens,
+                       int B, int Hkv, int d, int block_size, int num_blocks, pa_dtype dtype,
+                       int32_t* err_flag, void* stream);
+
+/*
+ * attn_decode_paged -- one query per sequence, attending over every cached
+ * key of that sequence through its block table (the query's own key
+ * included; no causal mask is needed), optionally limited to the last
+ * `window` keys. "Генерация и KV-кэш", section "KV-кэш для одной головы на
+ * NumPy" (decode_step); "Module 09: Efficient Attention", section "The Block
+ * Table" (gather by walking the table).
+ *
+ * Long contexts are split into ranges of blocks processed in parallel; each
+ * range yields a normalised partial output and its LSE, and a merge computes
+ * lse = ln sum_s e^{lse_s}, o = sum_s e^{lse_s - lse} o_s.
+ *
+ *  q          [B, Hq, d]
+ *  k_cache, v_cache [num_blocks, block_size, Hkv, d]
+ *  block_table int32 [B, max_blocks_per_seq]
+ *  seq_lens   int32 [B]: keys visible to each query (the current token's own
+ *             key included, so it must already be appended); 0 is allowed
+ *  o          [B, Hq, d] (same dtype as q)
+ *  lse        float32 [Hq, B] natural-log LSE; may be NULL
+ *  window     <= 0: all keys; > 0: only the last `window` keys
+ *  scale      <= 0: 1/sqrt(d)
+ *  num_splits 0: chosen by the library from B, the table width and the SM
+ *             count; > 0: the maximum number of ranges per sequence
+ *  workspace  device scratch of at least pa_decode_workspace_bytes(...)
+ *             bytes for the same arguments (may be NULL when that is 0)
+ * block_size must be 16. Alignment: q, o, pools 16-byte aligned; workspace
+ * 256-byte aligned.
+ */
+PA_API int pa_attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table, int max_blocks_per_seq,
+                         const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                         int d, int block_size, int num_blocks, int window, float scale,
+                         int num_splits, void* workspace, size_t workspace_bytes,
+                         pa_dtype dtype, int32_t* err_flag, void* stream);
+
+/*
+ * Workspace bytes attn_decode_paged needs for these arguments (0 when every
+ * sequence fits one range). Host-only arithmetic except that num_splits = 0
+ * reads the current device's SM count. Returns 0 on invalid arguments too.
+ */
+PA_API size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int max_blocks_per_seq,
+                                 int block_size, int window, int num_splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

@@ -1,0 +1,134 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads, exports
+every entry point the header declares, and rejects invalid arguments on the
+host before making any CUDA call."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from flashattention_paged_kv_fwd_b300 import build as pa_build
+from flashattention_paged_kv_fwd_b300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE = 0, 1, 2, 4
+FAKE = 0x10000  # an aligned address that is never dereferenced (checks fail first)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return binding.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PA_API[^;(]*?\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    for name in ("pa_attn_prefill", "pa_kv_append_paged", "pa_attn_decode_paged",
+                 "pa_decode_workspace_bytes", "pa_status_str"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (pa_\w+)$", out, flags=re.M))
+    for name in declared_symbols():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+    # nothing else leaks out of the C namespace
+    assert all(s in declared_symbols() for s in exported)
+
+
+def test_status_strings(lib):
+    assert lib.pa_status_str(0) == b"ok"
+    assert b"invalid" in lib.pa_status_str(1)
+    assert lib.pa_status_str(99) == b"unknown status"
+
+
+def _prefill(lib, **kw):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=4, Hkv=2, N=16, d=64,
+                cu=None, msl=0, causal=1, window=0, scale=0.0, dt=0, err=None, stream=None)
+    args.update(kw)
+    return lib.pa_attn_prefill(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                               args["Hq"], args["Hkv"], args["N"], args["d"], args["cu"],
+                               args["msl"], args["causal"], args["window"], args["scale"],
+                               args["dt"], args["err"], args["stream"])
+
+
+def test_prefill_host_validation(lib):
+    assert _prefill(lib, Hq=6, Hkv=4) == PA_ERR_INVALID_ARG       # Hkv must divide Hq
+    assert _prefill(lib, d=96) == PA_ERR_INVALID_ARG              # head dim 64 or 128
+    assert _prefill(lib, q=None) == PA_ERR_INVALID_ARG            # null pointer
+    assert _prefill(lib, q=FAKE + 8) == PA_ERR_INVALID_ARG        # 16-byte alignment
+    assert _prefill(lib, B=0) == PA_ERR_INVALID_ARG
+    assert _prefill(lib, dt=7) == PA_ERR_INVALID_ARG
+    assert _prefill(lib, causal=0, window=8) == PA_ERR_UNSUPPORTED
+    assert _prefill(lib, N=0) == PA_OK                            # nothing to do, no launch
+
+
+def _append(lib, **kw):
+    a = dict(kn=FAKE, vn=FAKE, kc=FAKE, vc=FAKE, table=FAKE, mb=4, sl=FAKE, cu=None, tn=2, B=2,
+             Hkv=2, d=64, bs=16, nb=8, dt=0, err=None, stream=None)
+    a.update(kw)
+    return lib.pa_kv_append_paged(a["kn"], a["vn"], a["kc"], a["vc"], a["table"], a["mb"], a["sl"],
+                                  a["cu"], a["tn"], a["B"], a["Hkv"], a["d"], a["bs"], a["nb"],
+                                  a["dt"], a["err"], a["stream"])
+
+
+def test_append_host_validation(lib):
+    assert _append(lib, tn=3) == PA_ERR_INVALID_ARG               # without cu_new, T_new = B
+    assert _append(lib, table=None) == PA_ERR_INVALID_ARG
+    assert _append(lib, kc=FAKE + 4) == PA_ERR_INVALID_ARG
+    assert _append(lib, d=32) == PA_ERR_INVALID_ARG
+    assert _append(lib, nb=0) == PA_ERR_INVALID_ARG
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, table=FAKE, mb=8, sl=FAKE, o=FAKE, lse=None, B=2, Hq=4,
+             Hkv=2, d=64, bs=16, nb=16, window=0, scale=0.0, ns=4, ws=None, wsb=0, dt=0,
+             err=None, stream=None)
+    a.update(kw)
+    return lib.pa_attn_decode_paged(a["q"], a["kc"], a["vc"], a["table"], a["mb"], a["sl"], a["o"],
+                                    a["lse"], a["B"], a["Hq"], a["Hkv"], a["d"], a["bs"], a["nb"],
+                                    a["window"], a["scale"], a["ns"], a["ws"], a["wsb"], a["dt"],
+                                    a["err"], a["stream"])
+
+
+def test_decode_host_validation(lib):
+    assert _decode(lib, Hq=5) == PA_ERR_INVALID_ARG
+    assert _decode(lib, bs=8) == PA_ERR_UNSUPPORTED                # pages of 16 tokens
+    assert _decode(lib, o=None) == PA_ERR_INVALID_ARG
+    # 4 ranges of 2 blocks need partial outputs: a missing workspace is refused
+    assert _decode(lib, ns=4, ws=None) == PA_ERR_WORKSPACE
+    assert _decode(lib, ns=4, ws=FAKE, wsb=16) == PA_ERR_WORKSPACE
+    assert _decode(lib, ns=4, ws=FAKE + 16, wsb=1 << 20) == PA_ERR_INVALID_ARG  # 256-B alignment
+    # bf16: at most 128 query heads per KV head at d = 128
+    assert _decode(lib, Hq=256, Hkv=1, d=128, ns=1) == PA_ERR_UNSUPPORTED
+
+
+def test_workspace_bytes_explicit_splits(lib):
+    f = lib.pa_decode_workspace_bytes
+    # B=2, Hq=4, d=64, 8 blocks in 4 ranges of 2: partial o (fp32) + lse, 256-B aligned parts
+    n = 2 * 4 * 4
+    assert f(2, 4, 2, 64, 8, 16, 0, 4) == (n * 64 * 4 + 255) // 256 * 256 + (n * 4 + 255) // 256 * 256
+    assert f(2, 4, 2, 64, 8, 16, 0, 1) == 0                       # one range: no partials
+    # a window of 20 tokens touches at most 3 blocks: 3 ranges of 1 block when 4 are asked
+    n3 = 2 * 4 * 3
+    assert f(2, 4, 2, 64, 8, 16, 20, 4) == (n3 * 64 * 4 + 255) // 256 * 256 + (n3 * 4 + 255) // 256 * 256
+    assert f(2, 5, 2, 64, 8, 16, 0, 4) == 0                       # invalid -> 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_LIB", None)
+    monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.load_library()
