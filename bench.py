@@ -1,0 +1,612 @@
+#!/usr/bin/env python
+"""Benchmark of the attention hot path on B300.
+
+Default step: one continuous-batching iteration of the window-4096 mixed
+batch (Hq=32, Hkv=8, d=128, bf16): a packed causal prefill of 16 prompts with
+lengths U[512, 4096], the append of all their K/V rows plus one new token for
+each of 240 decode requests into one shared paged pool, then a paged decode of
+those 240 requests (cached lengths U[1, 16384], last 4096 keys visible). That
+single step runs every kernel of the path: prefill (QK^T, masks, online
+softmax, PV, epilogue), paged append, paged decode and the split-KV merge.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. ``value`` is the decode phase's KV-read bandwidth
+(algorithmic bytes: keys and values of every visible token, read once), the
+first half of the metric; the prefill phase's TFLOP/s (algorithmic causal
+FLOPs, 4*d per visible query-key pair and query head) is the second half,
+under ``prefill``. Timing: CUDA events on the launching stream around each
+phase of each step, L2 flushed (512 MB written) before every step.
+
+``--impl reference`` times the CPU oracle (fp64, full score rows, naive block
+table walk) on a bounded sample of the same workload instead.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from flashattention_paged_kv_fwd_b300 import inputs  # noqa: E402
+
+METRIC = "paged GQA decode KV-read GB/s vs ~8 TB/s; causal prefill attention TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0}
+CSRC = os.path.join(ROOT, "flashattention_paged_kv_fwd_b300", "csrc")
+
+
+# ---------------------------------------------------------------- helpers
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixed_window4096",
+                    choices=["mixed_window4096", "gqa_decode_llama3_70b", "mha_decode_gpt2",
+                             "gqa_prefill_llama3_8b"],
+                    help="other workloads time a single kernel family (profiling aid)")
+    ap.add_argument("--only", choices=["prefill", "append", "decode"], default=None,
+                    help="run only one phase of the mixed step (profiling aid)")
+    ap.add_argument("--decode-batch", type=int, default=64,
+                    help="batch of gqa_decode_llama3_70b (smaller for profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.5,
+                    help="untimed seconds of steps before the timed region, sampled for clocks")
+    return ap.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_digest():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = sources_digest()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[2] == digest:
+                return int(parts[3])
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() in ("active", "1")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons,
+                "window": "untimed soak + timed region"}
+
+
+# ------------------------------------------------------------ work counts
+def prefill_flops(lengths, hq, d, window):
+    """4*d FLOPs (QK^T and PV, multiply-add = 2) per visible (query, key) pair
+    and query head; causal with an optional window."""
+    pairs = 0
+    for n in lengths:
+        if window > 0 and window < n:
+            w = window
+            pairs += w * (w + 1) // 2 + (n - w) * w
+        else:
+            pairs += n * (n + 1) // 2
+    return 4.0 * d * hq * pairs
+
+
+def decode_bytes(lengths, hkv, d, window, elem=2):
+    """Keys and values of every visible token, read once (2 * Hkv * d * elem per
+    token and sequence)."""
+    vis = sum(min(n, window) if window > 0 else n for n in lengths)
+    return float(vis) * 2 * hkv * d * elem
+
+
+def append_bytes(n_tokens, hkv, d, elem=2):
+    """Rows read from k_new/v_new and written into the pools."""
+    return float(n_tokens) * 2 * hkv * d * elem * 2
+
+
+# ----------------------------------------------------------------- steps
+class MixedStep:
+    """Device-resident inputs and the three calls of one mixed step."""
+
+    def __init__(self, device, binding):
+        self.b = binding
+        w = inputs.mixed_window4096(device)
+        self.w = w
+        pre = w["prefill"]
+        self.T = pre["q"].shape[0]
+        self.npf = w["n_prefill"]
+        self.table_dec = w["block_table"][self.npf:].contiguous()
+        self.k_cache, self.v_cache = w["k_cache"], w["v_cache"]
+        self.o_pre = torch.empty_like(pre["q"])
+        self.lse_pre = torch.empty((w["hq"], self.T), dtype=torch.float32, device=device)
+        self.o_dec = torch.empty_like(w["q_dec"])
+        self.lse_dec = torch.empty((w["hq"], w["n_decode"]), dtype=torch.float32, device=device)
+        need = binding.decode_workspace_bytes(w["n_decode"], w["hq"], w["hkv"], w["d"],
+                                              self.table_dec.shape[1], 16, w["window"])
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.err = binding.new_err_flag(device)
+        self.launches = {"prefill": 1, "append": 1, "decode": 2 if need > 0 else 1}
+        # the decode requests' new tokens must be in the pool before a decode-only run
+        self.append()
+        torch.cuda.synchronize()
+        self.flops = prefill_flops(w["prefill_lengths"], w["hq"], w["d"], w["window"])
+        self.dbytes = decode_bytes([c + 1 for c in w["cached_lengths"]], w["hkv"], w["d"],
+                                   w["window"])
+        self.abytes = append_bytes(w["k_new"].shape[0], w["hkv"], w["d"])
+
+    def prefill(self, q=None, k=None, v=None, cu=None):
+        w, pre = self.w, self.w["prefill"]
+        q = pre["q"] if q is None else q
+        k = w["k_new"][:self.T] if k is None else k
+        v = w["v_new"][:self.T] if v is None else v
+        self.b.attn_prefill(q, k, v, causal=True, window=w["window"],
+                            cu_seqlens=pre["cu_seqlens"] if cu is None else cu,
+                            max_seqlen=pre["max_seqlen"], out=self.o_pre, lse=self.lse_pre,
+                            err_flag=self.err)
+
+    def append(self, k_new=None, v_new=None, seq_lens=None, cu_new=None, table=None):
+        w = self.w
+        self.b.kv_append_paged(w["k_new"] if k_new is None else k_new,
+                               w["v_new"] if v_new is None else v_new,
+                               self.k_cache, self.v_cache,
+                               w["block_table"] if table is None else table,
+                               w["seq_lens_before"] if seq_lens is None else seq_lens,
+                               cu_new=w["cu_new"] if cu_new is None else cu_new, err_flag=self.err)
+
+    def decode(self, q=None, seq_lens=None, table=None):
+        w = self.w
+        self.b.attn_decode_paged(w["q_dec"] if q is None else q, self.k_cache, self.v_cache,
+                                 self.table_dec if table is None else table,
+                                 w["seq_lens_dec"] if seq_lens is None else seq_lens,
+                                 window=w["window"], out=self.o_dec, lse=self.lse_dec,
+                                 workspace=self.ws, err_flag=self.err)
+
+
+class SingleStep:
+    """A single-kernel workload (profiling aid): decode-only or prefill-only."""
+
+    def __init__(self, name, device, binding, decode_batch):
+        self.b = binding
+        self.name = name
+        self.err = binding.new_err_flag(device)
+        if name == "gqa_prefill_llama3_8b":
+            w = inputs.gqa_prefill_llama3_8b(device)
+            self.w = w
+            self.out = torch.empty_like(w["q"])
+            self.lse = torch.empty((w["hq"], w["q"].shape[0]), dtype=torch.float32, device=device)
+            self.flops = prefill_flops(w["lengths"], w["hq"], w["d"], 0)
+            self.dbytes = 0.0
+            self.phase = "prefill"
+            self.launches = {"prefill": 1}
+        else:
+            if name == "gqa_decode_llama3_70b":
+                w = inputs.gqa_decode_llama3_70b(device, batch=decode_batch)
+            else:
+                w = inputs.mha_decode_gpt2(device)
+            self.w = w
+            self.out = torch.empty_like(w["q"])
+            self.lse = torch.empty((w["hq"], w["q"].shape[0]), dtype=torch.float32, device=device)
+            need = binding.decode_workspace_bytes(w["q"].shape[0], w["hq"], w["hkv"], w["d"],
+                                                  w["block_table"].shape[1], 16, 0)
+            self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+            self.flops = 0.0
+            self.dbytes = decode_bytes(w["lengths"], w["hkv"], w["d"], 0)
+            self.phase = "decode"
+            self.launches = {"decode": 2 if need > 0 else 1}
+
+    def run(self):
+        w = self.w
+        if self.phase == "prefill":
+            self.b.attn_prefill(w["q"], w["k"], w["v"], causal=True, cu_seqlens=w["cu_seqlens"],
+                                max_seqlen=w["max_seqlen"], out=self.out, lse=self.lse,
+                                err_flag=self.err)
+        else:
+            self.b.attn_decode_paged(w["q"], w["k_cache"], w["v_cache"], w["block_table"],
+                                     w["seq_lens"], out=self.out, lse=self.lse, workspace=self.ws,
+                                     err_flag=self.err)
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(w, budget_s, on_device):
+    """Time the oracle on a bounded sample of the mixed workload: decode
+    requests in order until ``budget_s`` has passed, then the shortest prompt
+    (all rows). Returns GB/s (decode) and TFLOP/s (prefill) of the oracle."""
+    import oracle  # the CPU oracle: test infrastructure, used here only as a timed baseline
+
+    torch.set_num_threads(os.cpu_count() or 1)
+    c_len = w["cached_lengths"]
+    npf = w["n_prefill"]
+    table = w["block_table"]
+    cu_new = w["cu_new"].cpu().tolist()
+    window = w["window"]
+    done_bytes, t_dec, n_seq = 0.0, 0.0, 0
+    for i in range(w["n_decode"]):
+        b = npf + i
+        nblk = (c_len[i] + 1 + 15) // 16
+        ids = table[b, :nblk].long()
+        kc = w["k_cache"].index_select(0, ids).cpu()   # input slicing, not timed
+        vc = w["v_cache"].index_select(0, ids).cpu()
+        row = [list(range(nblk))]
+        kn = w["k_new"][cu_new[b]:cu_new[b] + 1].cpu()
+        vn = w["v_new"][cu_new[b]:cu_new[b] + 1].cpu()
+        q = w["q_dec"][i:i + 1].cpu()
+        t0 = time.perf_counter()
+        kc2, vc2 = oracle.append_paged(kc, vc, kn, vn, row, [c_len[i]], None, 16)
+        oracle.decode_paged(q, kc2, vc2, row, [c_len[i] + 1], block_size=16, window=window)
+        t_dec += time.perf_counter() - t0
+        done_bytes += decode_bytes([c_len[i] + 1], w["hkv"], w["d"], window)
+        n_seq += 1
+        if t_dec >= budget_s:
+            break
+    pre = w["prefill"]
+    lens = w["prefill_lengths"]
+    j = int(np.argmin(lens))
+    cu = pre["cu_seqlens"].cpu().tolist()
+    q = pre["q"][cu[j]:cu[j + 1]].cpu()
+    k = w["k_new"][cu[j]:cu[j + 1]].cpu()
+    v = w["v_new"][cu[j]:cu[j + 1]].cpu()
+    t0 = time.perf_counter()
+    oracle.sdpa(q, k, v, causal=True, window=window)
+    t_pre = time.perf_counter() - t0
+    flops = prefill_flops([lens[j]], w["hq"], w["d"], window)
+    return {
+        "decode_gbs": done_bytes / t_dec / 1e9,
+        "prefill_tflops": flops / t_pre / 1e12,
+        "sample": (f"{n_seq} of {w['n_decode']} decode requests (append + decode, "
+                   f"{done_bytes / 1e9:.3f} GB of visible KV, {t_dec:.1f} s) and prompt {j} "
+                   f"({lens[j]} tokens, all rows, {t_pre:.1f} s)"),
+        "cores": torch.get_num_threads(),
+        "seconds": t_dec + t_pre,
+    }
+
+
+# -------------------------------------------------------------- main arms
+def run_reference(args):
+    world, rank, local = dist_info()
+    if rank != 0:
+        return 0
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = inputs.mixed_window4096(dev, poison=False)
+    per_step_budget = 2.0
+    vals, pres, secs = [], [], []
+    sample = None
+    for step in range(args.warmup + args.steps):
+        r = oracle_sample(w, per_step_budget, dev != "cpu")
+        if step >= args.warmup:
+            vals.append(r["decode_gbs"])
+            pres.append(r["prefill_tflops"])
+            secs.append(r["seconds"])
+            sample = r
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "mixed_window4096", "hq": 32, "hkv": 8, "d": 128,
+                   "window": 4096, "prefill_requests": 16, "decode_requests": 240,
+                   "block_size": 16, "l2": "oracle on host cores"},
+        "prefill": {"value": statistics.median(pres), "unit": "TFLOP/s"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": sample["cores"],
+                         "kind": "oracle", "sample": sample["sample"]},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_steps(run_phase, phases, n, flush, stream):
+    """Run n steps; per phase, CUDA events on the launching stream. Returns
+    {phase: [ms per step]}."""
+    evs = []
+    for _ in range(n):
+        flush.zero_()
+        marks = [torch.cuda.Event(enable_timing=True)]
+        marks[0].record(stream)
+        for ph in phases:
+            run_phase(ph)
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            marks.append(e)
+        evs.append(marks)
+    torch.cuda.synchronize()
+    out = {ph: [] for ph in phases}
+    for marks in evs:
+        for i, ph in enumerate(phases):
+            out[ph].append(marks[i].elapsed_time(marks[i + 1]))
+    return out
+
+
+def run_ours(args):
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    from flashattention_paged_kv_fwd_b300 import binding
+
+    binding.load_library()
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    if args.workload == "mixed_window4096":
+        st = MixedStep(dev, binding)
+        phases = [args.only] if args.only else ["prefill", "append", "decode"]
+        run_phase = {"prefill": st.prefill, "append": st.append, "decode": st.decode}
+        call = lambda ph: run_phase[ph]()  # noqa: E731
+    else:
+        st = SingleStep(args.workload, dev, binding, args.decode_batch)
+        phases = [st.phase]
+        call = lambda ph: st.run()  # noqa: E731
+
+    # warm-up, then an untimed soak sampled for clocks, then the timed steps
+    time_steps(call, phases, args.warmup, flush, stream)
+    uuid = str(getattr(torch.cuda.get_device_properties(local), "uuid", ""))
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else (f"GPU-{uuid}" if uuid else local))
+    sampler.start()
+    t_soak = time.time()
+    while time.time() - t_soak < args.soak_s:
+        time_steps(call, phases, 5, flush, stream)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    times = time_steps(call, phases, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    binding.check_err_flag(st.err)
+
+    phase_ms = {ph: sum(v) / len(v) for ph, v in times.items()}
+    step_ms = sum(phase_ms.values())
+    if world > 1:
+        t = torch.tensor([phase_ms.get(p, 0.0) for p in ("prefill", "append", "decode")] +
+                         [step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        phase_ms = {p: float(t[i]) for i, p in enumerate(("prefill", "append", "decode"))
+                    if p in phase_ms}
+        step_ms = float(t[3])
+
+    # throughput per phase (whole job: all replicas' work over the slowest rank)
+    phases_out = {}
+    if "prefill" in phase_ms:
+        tf = world * st.flops / (phase_ms["prefill"] * 1e-3) / 1e12
+        phases_out["prefill"] = {"ms": phase_ms["prefill"], "value": tf, "unit": "TFLOP/s",
+                                 "work": st.flops, "launches": st.launches["prefill"]}
+    if "append" in phase_ms:
+        gb = world * st.abytes / (phase_ms["append"] * 1e-3) / 1e9
+        phases_out["append"] = {"ms": phase_ms["append"], "value": gb, "unit": "GB/s",
+                                "work": st.abytes, "launches": st.launches["append"]}
+    if "decode" in phase_ms:
+        gb = world * st.dbytes / (phase_ms["decode"] * 1e-3) / 1e9
+        phases_out["decode"] = {"ms": phase_ms["decode"], "value": gb, "unit": "GB/s",
+                                "work": st.dbytes, "launches": st.launches["decode"]}
+
+    # roofline of the kernel with the largest share of the step
+    dom = max(phase_ms, key=phase_ms.get)
+    roof = {}
+    for ph, info in phases_out.items():
+        if ph == "prefill":
+            peak = peaks["bf16_tflops"]
+            r = {"bound": "tensor", "achieved": info["value"] / world, "peak": peak,
+                 "unit": "TFLOP/s"}
+        else:
+            peak = peaks["hbm_gbs"]
+            r = {"bound": "hbm", "achieved": info["value"] / world, "peak": peak, "unit": "GB/s"}
+        r["frac"] = r["achieved"] / r["peak"]
+        r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" \
+            else "fallback (recipe)"
+        kname = {"prefill": "prefill_bf16", "append": "kv_append", "decode": "decode_bf16"}[ph]
+        r["traffic"] = recorded_traffic(kname, args.workload)
+        r["kernel_share"] = phase_ms[ph] / step_ms
+        roof[ph] = r
+
+    # end to end: the same calls from pinned host buffers, copies inside the region
+    e2e = None
+    if not args.no_e2e and args.workload == "mixed_window4096" and not args.only:
+        e2e = run_e2e(st, args, stream, flush, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and \
+            args.workload == "mixed_window4096":
+        r = oracle_sample(st.w, 12.0, True)
+        cpu = {"value": r["decode_gbs"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+               "sample": r["sample"], "prefill_tflops": r["prefill_tflops"]}
+
+    if args.workload == "mixed_window4096":
+        head = "decode" if "decode" in phases_out else list(phases_out)[0]
+    else:
+        head = st.phase
+    value = phases_out[head]["value"]
+    unit = phases_out[head]["unit"]
+    launches = args.steps * sum(st.launches[p] for p in phases)
+    cfg = {"workload": args.workload}
+    if args.workload == "mixed_window4096":
+        w = st.w
+        cfg.update({"hq": 32, "hkv": 8, "d": 128, "window": w["window"], "block_size": 16,
+                    "prefill_requests": w["n_prefill"], "prefill_tokens": st.T,
+                    "decode_requests": w["n_decode"],
+                    "decode_visible_tokens": int(st.dbytes // (2 * 8 * 128 * 2)),
+                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                    "l2": "flushed before every step (512 MB write)"})
+        if args.only:
+            cfg["only"] = args.only
+    else:
+        cfg.update({"l2": "flushed before every step (512 MB write)"})
+    line = {
+        "metric": METRIC if args.workload == "mixed_window4096" else
+        {"prefill": "causal prefill attention TFLOP/s", "decode": "paged decode KV-read GB/s"}[head],
+        "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": cfg,
+        "prefill": phases_out.get("prefill"),
+        "phases": phases_out,
+        "roofline": roof[dom],
+        "roofline_by_phase": roof,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(st, args, stream, flush, world):
+    """Host -> device copies of the step's inputs from pinned memory, the three
+    calls, and device -> host copies of the outputs, all inside the events."""
+    w = st.w
+    pre = w["prefill"]
+    host = {
+        "q": pre["q"].cpu().pin_memory(), "k_new": w["k_new"].cpu().pin_memory(),
+        "v_new": w["v_new"].cpu().pin_memory(), "cu": pre["cu_seqlens"].cpu().pin_memory(),
+        "cu_new": w["cu_new"].cpu().pin_memory(),
+        "seq_before": w["seq_lens_before"].cpu().pin_memory(),
+        "table": w["block_table"].cpu().pin_memory(), "q_dec": w["q_dec"].cpu().pin_memory(),
+        "seq_dec": w["seq_lens_dec"].cpu().pin_memory(),
+    }
+    dev = {k: torch.empty_like(v, device=w["q_dec"].device) for k, v in host.items()}
+    outs = {"o_pre": torch.empty(st.o_pre.shape, dtype=st.o_pre.dtype).pin_memory(),
+            "lse_pre": torch.empty(st.lse_pre.shape).pin_memory(),
+            "o_dec": torch.empty(st.o_dec.shape, dtype=st.o_dec.dtype).pin_memory(),
+            "lse_dec": torch.empty(st.lse_dec.shape).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def one():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        T = st.T
+        st.prefill(dev["q"], dev["k_new"][:T], dev["v_new"][:T], dev["cu"])
+        st.append(dev["k_new"], dev["v_new"], dev["seq_before"], dev["cu_new"], dev["table"])
+        st.decode(dev["q_dec"], dev["seq_dec"], dev["table"][st.npf:])
+        outs["o_pre"].copy_(st.o_pre, non_blocking=True)
+        outs["lse_pre"].copy_(st.lse_pre, non_blocking=True)
+        outs["o_dec"].copy_(st.o_dec, non_blocking=True)
+        outs["lse_dec"].copy_(st.lse_dec, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    step = sum(ms) / len(ms)
+    return {"value": world * st.dbytes / (step * 1e-3) / 1e9, "unit": "GB/s",
+            "basis": "decode KV bytes / whole step time (copies + prefill + append + decode)",
+            "ms_per_step": step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -32,7 +32,8 @@ def assert_close(got, want, what, tol):
     g, w = to64(got), to64(want)
     assert g.shape == w.shape, (what, g.shape, w.shape)
     both_inf = np.isneginf(g) & np.isneginf(w)
-    d = np.where(both_inf, 0.0, np.abs(g - w))
+    with np.errstate(invalid="ignore"):
+        d = np.where(both_inf, 0.0, np.abs(g - w))
     assert np.isfinite(d).all(), f"{what}: non-finite mismatch"
     assert d.max() <= tol, f"{what}: max |d| = {d.max():.3e} > {tol}"
 

@@ -92,7 +92,8 @@ def test_mixed_continuous_batch_full_size():
     c_len = w["cached_lengths"]
     picks = sorted({0, int(np.argmax(c_len)), int(np.argmin(c_len)), 123, 239})
     caps = [c_len[i] + 1 for i in picks]
-    k0, v0, table = mini_pool(w["k_cache"], w["v_cache"], table_dec, picks, caps)
+    k0, v0, table = mini_pool(w["k_cache"], w["v_cache"], table_dec, picks,
+                              [c + 1 for c in c_len])
     k1, v1 = oracle.append_paged(k0, v0, w["k_new"][[cu[-1] + i for i in picks]].cpu(),
                                  w["v_new"][[cu[-1] + i for i in picks]].cpu(), table,
                                  [c_len[i] for i in picks], None, 16)
