@@ -84,9 +84,17 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def sources_digest():
+# Sources whose change invalidates a kernel's recorded DRAM traffic.
+KERNEL_SOURCES = {
+    "prefill_bf16": ("prefill_sm103.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
+    "decode_bf16": ("decode_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
+    "kv_append": ("append_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
+}
+
+
+def sources_digest(kernel):
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -98,7 +106,7 @@ def recorded_traffic(kernel, workload):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = sources_digest()
+    digest = sources_digest(kernel)
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -195,26 +203,28 @@ def append_bytes(n_tokens, hkv, d, elem=2):
 class MixedStep:
     """Device-resident inputs and the three calls of one mixed step."""
 
-    def __init__(self, device, binding):
+    def __init__(self, device, binding, with_cache=True):
         self.b = binding
-        w = inputs.mixed_window4096(device)
+        w = inputs.mixed_window4096(device, with_cache=with_cache)
         self.w = w
         pre = w["prefill"]
         self.T = pre["q"].shape[0]
         self.npf = w["n_prefill"]
-        self.table_dec = w["block_table"][self.npf:].contiguous()
+        self.table_dec = w["block_table"][self.npf:].contiguous() if with_cache else None
         self.k_cache, self.v_cache = w["k_cache"], w["v_cache"]
         self.o_pre = torch.empty_like(pre["q"])
         self.lse_pre = torch.empty((w["hq"], self.T), dtype=torch.float32, device=device)
         self.o_dec = torch.empty_like(w["q_dec"])
         self.lse_dec = torch.empty((w["hq"], w["n_decode"]), dtype=torch.float32, device=device)
+        width = self.table_dec.shape[1] if with_cache else 1025
         need = binding.decode_workspace_bytes(w["n_decode"], w["hq"], w["hkv"], w["d"],
-                                              self.table_dec.shape[1], 16, w["window"])
+                                              width, 16, w["window"])
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         self.err = binding.new_err_flag(device)
         self.launches = {"prefill": 1, "append": 1, "decode": 2 if need > 0 else 1}
         # the decode requests' new tokens must be in the pool before a decode-only run
-        self.append()
+        if with_cache:
+            self.append()
         torch.cuda.synchronize()
         self.flops = prefill_flops(w["prefill_lengths"], w["hq"], w["d"], w["window"])
         self.dbytes = decode_bytes([c + 1 for c in w["cached_lengths"]], w["hkv"], w["d"],
@@ -420,7 +430,8 @@ def run_ours(args):
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     if args.workload == "mixed_window4096":
-        st = MixedStep(dev, binding)
+        # a prefill-only run needs no KV pools (keeps profiler captures small)
+        st = MixedStep(dev, binding, with_cache=args.only != "prefill")
         phases = [args.only] if args.only else ["prefill", "append", "decode"]
         run_phase = {"prefill": st.prefill, "append": st.append, "decode": st.decode}
         call = lambda ph: run_phase[ph]()  # noqa: E731

@@ -190,13 +190,14 @@ def gqa_decode_llama3_70b(device="cpu", dtype=torch.bfloat16, poison=True, batch
 
 def mixed_window4096(device="cpu", dtype=torch.bfloat16, poison=True, n_prefill=16,
                      n_decode=240, prefill_lo=512, prefill_hi=4096, cached_lo=1,
-                     cached_hi=16384, window=4096):
+                     cached_hi=16384, window=4096, with_cache=True):
     """One continuous-batching step over a shared pool (window 4096).
 
     Sequences 0..n_prefill-1 are fresh prompts: their packed q/k/v go through
     the prefill kernel and all their tokens are appended. Sequences
     n_prefill.. are decode requests holding ``cached`` tokens: each appends
-    one token, then decodes with seq_len = cached + 1.
+    one token, then decodes with seq_len = cached + 1. ``with_cache=False``
+    skips the pools and block table (the other inputs are drawn identically).
     """
     seed = WORKLOAD_SEEDS["mixed_window4096"]
     hq, hkv, d = 32, 8, 128
@@ -210,7 +211,12 @@ def mixed_window4096(device="cpu", dtype=torch.bfloat16, poison=True, n_prefill=
     v_dec = randn((n_decode, hkv, d), dtype, gen, device)
     capacities = p_len + [c + 1 for c in c_len]
     filled = [0] * n_prefill + c_len
-    cache = make_paged_cache(capacities, filled, hkv, d, dtype, seed + 1, device, poison=poison)
+    if with_cache:
+        cache = make_paged_cache(capacities, filled, hkv, d, dtype, seed + 1, device,
+                                 poison=poison)
+    else:
+        cache = {"k_cache": None, "v_cache": None, "block_table": None, "num_blocks": 0,
+                 "block_size": BLOCK_SIZE}
     cu_new = [0]
     for n in p_len + [1] * n_decode:
         cu_new.append(cu_new[-1] + n)
