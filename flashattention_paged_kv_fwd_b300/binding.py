@@ -241,3 +241,46 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, *, window=0, s
 
 def default_scale(head_dim):
     return 1.0 / math.sqrt(head_dim)
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def _noalloc_fn():
+    lib = load_library()
+    fn = lib.pa_attn_decode_paged_noalloc
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                   i32, vp, vp]
+    fn.restype = i32
+    return fn
+
+
+def attn_decode_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, out, lse=None, *,
+                              window=0, scale=None, num_splits=0, err_flag=None, stream=None):
+    """attn_decode_paged for callers that cannot allocate device memory.
+
+    The caller passes the output ``out`` [B, Hq, d] (and optionally ``lse``
+    [Hq, B]); the split-KV partials use the library's built-in scratch of
+    NOALLOC_SCRATCH_BYTES per GPU, so neither this wrapper nor the library
+    allocates. Calls whose partials would not fit raise PagedAttnError
+    (use a smaller ``num_splits``); calls that overlap on the GPU share the
+    scratch and must be ordered on one stream.
+    """
+    _need(q.dtype in _DTYPES, "q must be bfloat16 or float32")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        _cuda_contig(name, t, q.dtype)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("seq_lens", seq_lens, torch.int32)
+    B, hq, d = q.shape
+    num_blocks, block_size, hkv, _ = k_cache.shape
+    _need(out.shape == q.shape, "out must match q")
+    if lse is not None:
+        _cuda_contig("lse", lse, torch.float32)
+        _need(lse.shape == (hq, B), "lse must be [Hq, B]")
+    st = _noalloc_fn()(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                       block_table.shape[1], _ptr(seq_lens), _ptr(out), _ptr(lse), B, hq, hkv, d,
+                       block_size, num_blocks, int(window or 0), float(scale or 0.0),
+                       int(num_splits), _DTYPES[q.dtype], _ptr(err_flag), _stream(stream))
+    _check(st, "attn_decode_paged_noalloc")
+    return out, lse

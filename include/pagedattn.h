@@ -175,6 +175,40 @@ PA_API int pa_attn_decode_paged(const void* q, const void* k_cache, const void* 
 PA_API size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int max_blocks_per_seq,
                                  int block_size, int window, int num_splits);
 
+/* Bytes of the library's built-in decode scratch (see below): 32 MiB. */
+#define PA_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)
+
+/*
+ * attn_decode_paged_noalloc -- the same paged decode as attn_decode_paged
+ * (same arguments, same kernels, same results) without the workspace
+ * arguments. The pages have no counterpart: this entry point exists for
+ * callers that cannot allocate device memory when they call it, such as a
+ * serving process that reserves its whole memory budget at start-up and must
+ * not allocate afterwards, or a plugin that only receives buffers from a host
+ * framework that owns all device allocations.
+ *
+ * The split-KV partial outputs go to a scratch array compiled into the
+ * library: PA_NOALLOC_SCRATCH_BYTES per GPU, held by every GPU that loads the
+ * library until the process exits. The call allocates nothing.
+ *  - A call whose partials need more than PA_NOALLOC_SCRATCH_BYTES
+ *    (pa_decode_workspace_bytes for the same arguments) returns
+ *    PA_ERR_WORKSPACE and launches nothing; pass a smaller num_splits (1 needs
+ *    no scratch at all).
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture. PA_ERR_CUDA if the lookup fails.
+ *  - All calls on a device share the one array, which keeps whatever the last
+ *    call left there (nothing in it needs to start at zero). Calls that can
+ *    overlap on the GPU -- on different streams, or from different host
+ *    threads -- race on it; order them on one stream.
+ */
+PA_API int pa_attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, int max_blocks_per_seq,
+                                        const int32_t* seq_lens, void* o, float* lse, int B,
+                                        int Hq, int Hkv, int d, int block_size, int num_blocks,
+                                        int window, float scale, int num_splits, pa_dtype dtype,
+                                        int32_t* err_flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
