@@ -141,7 +141,7 @@ int pa_attn_prefill(const void* q, const void* k, const void* v, void* o, float*
     if (!encode_3d(&qm, q, d, Hq, T, 128) || !encode_3d(&km, k, d, Hkv, T, 128) ||
         !encode_3d(&vm, v, d, Hkv, T, 128))
       return PA_ERR_CUDA;
-    e = pa::launch_prefill_bf16(a, qm, km, vm, s);
+    e = pa::launch_prefill_bf16(a, qm, km, vm, sm_count(), s);
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -65,10 +65,15 @@ struct PrefillArgs {
   int32_t* err;
   int B, Hq, Hkv, N, T, d, max_seqlen, causal, window;
   float scale_log2;
+  int pair_heads;  // bf16 path: a work unit pairs two query heads (else two row tiles)
+  int n_units;     // bf16 path: work units in the launch
 };
 
+// Work units of the bf16 prefill (two 128-row query tiles each).
+long long prefill_units(int B, int Hq, int Hkv, int max_seqlen, bool* pair_heads);
+
 cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& qmap,
-                                const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                const CUtensorMap& kmap, const CUtensorMap& vmap, int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_prefill_f32(const PrefillArgs& a, cudaStream_t s);
 

@@ -114,6 +114,18 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A (M rows x 16 bf16) is read
+// from TMEM, lane = row, each 32-bit column holding two consecutive k values
+// (the lower k in the low half); B comes from a shared-memory descriptor.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive (once) on an mbarrier when all previously issued tcgen05 ops of this
 // thread have completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -202,6 +214,122 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------- packed fp32 pairs (sm_100 family)
+// Two fp32 lanes in one 64-bit register; one instruction operates on both.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (NaN-free inputs here: scores or -inf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// ------------------------------------- whole-warp tcgen05 issue (one elected lane)
+// Every lane of a converged warp executes these; elect.sync picks the same
+// lane (the lowest) each time, so that lane's commits track its own MMAs.
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+      "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
+}
+// S = Q K^T for d = 128: eight 16-wide k-steps. a / b are the descriptors of
+// the first step; a step advances 32 bytes inside a 128-byte panel row (2 in
+// descriptor units) and the second 64-column panel starts 16 KB further
+// (1024 units).
+__device__ __forceinline__ void umma_ss_k128_elect(uint32_t d, uint64_t a, uint64_t b,
+                                                   uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b64 a1, b1;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "add.s64 a1, %1, 1024;\n\tadd.s64 b1, %2, 1024;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "add.s64 a1, %1, 1026;\n\tadd.s64 b1, %2, 1026;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "add.s64 a1, %1, 1028;\n\tadd.s64 b1, %2, 1028;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "add.s64 a1, %1, 1030;\n\tadd.s64 b1, %2, 1030;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc)
+      : "memory");
+}
+// Same for d = 64: four k-steps inside one panel.
+__device__ __forceinline__ void umma_ss_k64_elect(uint32_t d, uint64_t a, uint64_t b,
+                                                  uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b64 a1, b1;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc)
+      : "memory");
+}
+// O (+)= P V over 128 keys: P is read from TMEM (8 columns per 16 keys), V's
+// 16-row k-steps are 2 KB apart (128 descriptor units). `acc` = 0 makes the
+// first step overwrite O.
+__device__ __forceinline__ void umma_ts_k128_elect(uint32_t d, uint32_t p, uint64_t b,
+                                                   uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred P, A;\n\t.reg .b64 b1;\n\t.reg .b32 p1;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "setp.ne.b32 A, %4, 0;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, A;\n\t"
+      "add.s32 p1, %1, 8;\n\tadd.s64 b1, %2, 128;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
+      "add.s32 p1, %1, 16;\n\tadd.s64 b1, %2, 256;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
+      "add.s32 p1, %1, 24;\n\tadd.s64 b1, %2, 384;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
+      "add.s32 p1, %1, 32;\n\tadd.s64 b1, %2, 512;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
+      "add.s32 p1, %1, 40;\n\tadd.s64 b1, %2, 640;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
+      "add.s32 p1, %1, 48;\n\tadd.s64 b1, %2, 768;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
+      "add.s32 p1, %1, 56;\n\tadd.s64 b1, %2, 896;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
+      "}" ::"r"(d),
+      "r"(p), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {

@@ -13,28 +13,44 @@
 // included); GQA head mapping as in the notebook's section "The Math: Sharing
 // Keys and Values".
 //
-// sm_103a design (one 128-row query tile of one head per CTA):
-//  * warp 0, one thread: TMA producer. Q tile once; K and V tiles of 128 keys
-//    through a `NS`-deep ring. Every tile is stored as 64-element (128-byte)
-//    panels, 128-byte swizzled, which is the K-major / MN-major operand layout
-//    the tensor cores read directly.
-//  * warp 1, one thread: tcgen05.mma issuer. S_j = Q K_j^T (M=128, N=128,
-//    bf16 x bf16 -> fp32) into one of two TMEM score buffers, then
-//    O += P_{j-1} V_{j-1} (M=128, N=d) into a TMEM accumulator, so the tensor
-//    cores compute the next scores while the softmax works on the current ones.
-//    Completion is signalled with tcgen05.commit on mbarriers.
-//  * warps 2-5 (128 threads, one query row each): load the row's scores from
-//    TMEM, mask only on tiles that straddle the diagonal, the window edge or
-//    the sequence end, update the running max in the log2 domain with
-//    scale*log2(e) folded into one FMA, exponentiate with ex2, write P (bf16)
-//    to shared memory in the swizzled A-operand layout, and at the end read O
-//    back from TMEM, divide by the running sum and store O and the LSE.
+// sm_103a design. A persistent grid of one CTA per SM walks a static list of
+// work units, heaviest first. A unit is two 128-row query tiles that read the
+// same K/V stream: the same rows of two query heads of one KV group when
+// Hq/Hkv is even, otherwise two consecutive row tiles of one head (their key
+// ranges are merged; keys a tile may not see are masked).
+//  * warp 8 (TMA producer): the unit's two Q tiles, then K and V tiles of 128
+//    keys in turn through a ring of 32 KB slots (d = 128). Every tile is
+//    stored as 64-element (128-byte) panels, 128-byte swizzled: the K-major /
+//    MN-major operand layouts the tensor cores read directly.
+//  * warp 9 (tcgen05 issuer): MMAs in the steady order
+//      ... QK_0(j), PV_1(j-1), QK_1(j), PV_0(j), QK_0(j+1), PV_1(j), ...
+//    S_i = Q_i K^T (M=128, N=128, both operands in shared memory) into TMEM,
+//    and O_i += P_i V (A = P_i read from TMEM, B = V in shared memory). Each
+//    softmax therefore has two other MMAs (about 1000 cycles) to run in, and
+//    the two softmax warpgroups take turns on the SFU. Descriptors are formed
+//    once; the per-MMA issue work is one add, which keeps the MMA pipe full.
+//  * warps 0-3 / 4-7 (softmax of query tile 0 / 1, one row per thread): read
+//    the row's 128 scores from TMEM, mask only on tiles that straddle the
+//    diagonal, the window edge or the sequence end, update the running max in
+//    the log2 domain with scale*log2(e) folded into one FMA, exponentiate with
+//    ex2, and write P as bf16 pairs back into the first 64 columns of the same
+//    TMEM score buffer, where the PV MMA reads it. At the end of a unit they
+//    read O from TMEM, divide by the running sum and store O and the LSE.
 //  * The max is rescaled lazily: O and the sum are only rescaled when the max
-//    grows by more than 2^8, otherwise the stale max is kept. The final O / sum
-//    is unchanged (both carry the same factor), P stays <= 256, and TMEM
-//    round trips of O become rare.
-//  * Tiles above the diagonal or left of the window are never loaded; CTAs
-//    are launched heaviest query tile first to even out the causal triangle.
+//    grows by more than 2^8; otherwise the stale max is kept. O / sum is
+//    unchanged (both carry the same factor), P stays <= 256, and TMEM round
+//    trips of O become rare. When a softmax sees S_i(j), the commit that
+//    signalled it also covers PV_i(j-1), so O_i is idle until P_i(j) is
+//    handed over and the rescale needs no extra wait.
+//  * S_i(j+1) overwrites the TMEM columns that hold P_i(j). The MMA that
+//    reads P_i(j) is issued before the MMA that overwrites it, by the same
+//    thread, and the SM's tensor core executes one thread's MMAs in issue
+//    order.
+//  * Tiles above the diagonal or left of the window are never loaded. All
+//    waits are bounded; a wait that gives up raises PA_DEV_TIMEOUT, and every
+//    role then winds down: copies and MMAs in flight are waited for before
+//    TMEM is freed.
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -53,95 +69,154 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 256x
 
-template <int D>
-struct PfCfg {
-  static constexpr int P = D / 64;                   // 128-byte panels per row
-  static constexpr int NS = (D == 128) ? 2 : 4;      // K/V ring depth
-  static constexpr int QB = BM * D * 2;              // Q tile bytes
-  static constexpr int KB = BN * D * 2;              // one K (or V) tile
-  static constexpr int PB = BM * BN * 2;             // P tile (bf16)
-  static constexpr int QPANEL = BM * 128;            // bytes per Q / P panel
-  static constexpr int KPANEL = BN * 128;            // bytes per K / V panel
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + QB;
-  static constexpr int OFF_V = OFF_K + NS * KB;
-  static constexpr int OFF_P = OFF_V + NS * KB;
-  static constexpr int OFF_BAR = OFF_P + PB;
-  // barriers
-  static constexpr int B_QFULL = 0;
-  static constexpr int B_KFULL = 1;                  // + stage
-  static constexpr int B_KEMPTY = 1 + NS;
-  static constexpr int B_VFULL = 1 + 2 * NS;
-  static constexpr int B_VEMPTY = 1 + 3 * NS;
-  static constexpr int B_SFULL = 1 + 4 * NS;         // + buffer (2)
-  static constexpr int B_SFREE = 3 + 4 * NS;         // + buffer (2)
-  static constexpr int B_PFULL = 5 + 4 * NS;
-  static constexpr int B_ODONE = 6 + 4 * NS;
-  static constexpr int B_DRAIN = 7 + 4 * NS;
-  static constexpr int NBAR = 8 + 4 * NS;
-  static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
-  static constexpr uint32_t TMEM_COLS = 512;         // S0 | S1 | O
-  static constexpr uint32_t TM_S0 = 0, TM_S1 = BN, TM_O = 2 * BN;
-};
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;  // 8 softmax warps + producer + MMA issuer
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+struct PfCfg {
+  static constexpr int QB = BM * D * 2;        // one Q tile (bytes)
+  static constexpr int TB = BN * D * 2;        // one K or V tile
+  static constexpr int PANEL_Q = BM * 128;     // bytes per 64-column panel of a Q tile
+  static constexpr int PANEL_T = BN * 128;     // of a K / V tile
+  static constexpr int NSLOT = D == 128 ? 5 : 10;  // K/V ring slots
+  static constexpr int OFF_Q = 0;              // Q tile 0, Q tile 1
+  static constexpr int OFF_RING = 2 * QB;
+  static constexpr int OFF_BAR = OFF_RING + NSLOT * TB;
+  // mbarriers
+  static constexpr int B_QFULL = 0;            // + query tile
+  static constexpr int B_QFREE = 2;            // + query tile
+  static constexpr int B_FULL = 4;             // + ring slot
+  static constexpr int B_EMPTY = 4 + NSLOT;    // + ring slot
+  static constexpr int B_SFULL = 4 + 2 * NSLOT;   // + query tile
+  static constexpr int B_PRDY = 6 + 2 * NSLOT;    // + query tile
+  static constexpr int B_OFULL = 8 + 2 * NSLOT;   // + query tile
+  static constexpr int B_DRAIN = 10 + 2 * NSLOT;
+  static constexpr int NBAR = 11 + 2 * NSLOT;
+  static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TM_O = 2 * BN;     // S_i at i*BN, O_i at TM_O + i*D
+};
+static_assert(PfCfg<128>::SMEM <= 227 * 1024, "prefill d=128 shared memory");
+static_assert(PfCfg<128>::PANEL_Q == PfCfg<128>::PANEL_T, "Q and K panels share descriptor offsets");
+static_assert(PfCfg<64>::SMEM <= 227 * 1024, "prefill d=64 shared memory");
+
+// One work unit: two query tiles sharing a KV head and a key range.
+struct Unit {
+  int start, len;  // packed row offset and length of the sequence
+  int q0[2];       // first row (within the sequence) of each query tile
+  int h[2];        // query head of each tile
+  int kvh;
+  int t_begin;     // first key tile
+  int n_tiles;     // key tiles streamed
+};
+
+__device__ __forceinline__ bool decode_unit(const PrefillArgs& a, int u, Unit& w) {
+  const int n_qt = (a.max_seqlen + BM - 1) / BM;
+  int qt0, qt1, b;
+  if (a.pair_heads) {
+    const int per = (a.Hq >> 1) * a.B;
+    const int lvl = u / per, rem = u - lvl * per;
+    b = rem % a.B;
+    const int hp = rem / a.B;
+    qt0 = qt1 = a.causal ? n_qt - 1 - lvl : lvl;
+    w.h[0] = 2 * hp;
+    w.h[1] = 2 * hp + 1;
+  } else {
+    const int n_qp = (n_qt + 1) >> 1;
+    const int per = a.Hq * a.B;
+    const int lvl = u / per, rem = u - lvl * per;
+    b = rem % a.B;
+    const int h = rem / a.B;
+    const int qp = a.causal ? n_qp - 1 - lvl : lvl;
+    qt0 = 2 * qp;
+    qt1 = qt0 + 1;
+    w.h[0] = w.h[1] = h;
+  }
+  if (a.cu_seqlens) {
+    w.start = a.cu_seqlens[b];
+    w.len = a.cu_seqlens[b + 1] - w.start;
+  } else {
+    w.start = b * a.N;
+    w.len = a.N;
+  }
+  w.q0[0] = qt0 * BM;
+  w.q0[1] = qt1 * BM;
+  if (w.q0[0] >= w.len) return false;
+  const int q_last = min(w.len, w.q0[1] + BM) - 1;  // last row of either tile
+  const int kv_end = a.causal ? q_last + 1 : w.len;
+  const int kv_begin = a.window > 0 ? max(0, w.q0[0] - a.window + 1) : 0;
+  w.t_begin = kv_begin / BN;
+  w.n_tiles = (kv_end + BN - 1) / BN - w.t_begin;
+  w.kvh = w.h[0] / (a.Hq / a.Hkv);
+  return true;
+}
+
+// Unit of the k-th round of CTA c: rounds alternate direction ("snake"), so
+// with units sorted heaviest first every CTA gets a similar total.
+__device__ __forceinline__ int unit_of(int k, int c, int G) {
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Every lane of the warp waits; the outcome is made warp-uniform so that a
+// give-up seen by one lane ends the loops of all 32 together (the warp-wide
+// tcgen05 and shuffle instructions that follow need every lane).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag) {
+  const bool ok = pf_wait(bar, parity, abort_flag);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for copies / MMAs already in flight
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
 prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   using C = PfCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ------------------------------------------------------- tile -> work item
-  const int n_qt = (a.max_seqlen + BM - 1) / BM;
-  const int per = a.Hq * a.B;
-  const int qt_r = blockIdx.x / per, hb = blockIdx.x % per;
-  const int h = hb % a.Hq, b = hb / a.Hq;
-  const int qt = a.causal ? (n_qt - 1 - qt_r) : qt_r;  // heaviest tiles first
-  int start, len;
-  if (a.cu_seqlens) {
-    start = a.cu_seqlens[b];
-    len = a.cu_seqlens[b + 1] - start;
-  } else {
-    start = b * a.N;
-    len = a.N;
-  }
-  const int q0 = qt * BM;
-  if (q0 >= len) return;
-  const int rows = min(BM, len - q0);
-  const int q_last = q0 + rows - 1;
-  const int kv_end = a.causal ? q_last + 1 : len;
-  const int kv_begin = a.window > 0 ? max(0, q0 - a.window + 1) : 0;
-  const int t_begin = kv_begin / BN;
-  const int n_tiles = (kv_end + BN - 1) / BN - t_begin;
-  const int kvh = h / (a.Hq / a.Hkv);
+  const int G = gridDim.x, cta = blockIdx.x;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (base - raw);
-  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V,
-                 sP = base + C::OFF_P;
+  const uint32_t sQ = base + C::OFF_Q, sRing = base + C::OFF_RING;
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     if (lane == 0) {
-      mbar_init(bar(C::B_QFULL), 1);
-      for (int i = 0; i < C::NS; ++i) {
-        mbar_init(bar(C::B_KFULL + i), 1);
-        mbar_init(bar(C::B_KEMPTY + i), 1);
-        mbar_init(bar(C::B_VFULL + i), 1);
-        mbar_init(bar(C::B_VEMPTY + i), 1);
-      }
       for (int i = 0; i < 2; ++i) {
+        mbar_init(bar(C::B_QFULL + i), 1);
+        mbar_init(bar(C::B_QFREE + i), 1);
         mbar_init(bar(C::B_SFULL + i), 1);
-        mbar_init(bar(C::B_SFREE + i), 128);
+        mbar_init(bar(C::B_PRDY + i), 128);
+        mbar_init(bar(C::B_OFULL + i), 1);
       }
-      mbar_init(bar(C::B_PFULL), 128);
-      mbar_init(bar(C::B_ODONE), 1);
+      for (int s = 0; s < C::NSLOT; ++s) {
+        mbar_init(bar(C::B_FULL + s), 1);
+        mbar_init(bar(C::B_EMPTY + s), 1);
+      }
       mbar_init(bar(C::B_DRAIN), 1);
       *abort_flag = 0;
       fence_mbar_init();
@@ -155,222 +230,319 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    const bool leader = lane == 0;
+    if (leader) {
       prefetch_tmap(&qmap);
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
-      mbar_arrive_expect_tx(bar(C::B_QFULL), C::QB);
+    }
+    uint32_t slot = 0, phase = 0;
+    int issued = 0;             // K/V tiles issued into the ring
+    int q_loads = 0;            // units whose Q tiles were issued
+    bool ok = true;
+    auto load_tile = [&](const CUtensorMap* m, int row, int head) -> bool {
+      if (issued >= C::NSLOT && !warp_wait(bar(C::B_EMPTY + slot), phase ^ 1u, abort_flag))
+        return false;
+      if (leader) {
+        const uint32_t fb = bar(C::B_FULL + slot);
+        mbar_arrive_expect_tx(fb, C::TB);
 #pragma unroll
-      for (int p = 0; p < C::P; ++p)
-        tma_load_3d(sQ + p * C::QPANEL, &qmap, bar(C::B_QFULL), p * 64, h, start + q0);
-      int issued = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int st = it % C::NS, u = it / C::NS;
-        const int krow = start + (t_begin + it) * BN;
-        if (u > 0 && !mbar_wait(bar(C::B_KEMPTY + st), (u - 1) & 1)) break;
-        mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::KB);
-#pragma unroll
-        for (int p = 0; p < C::P; ++p)
-          tma_load_3d(sK + st * C::KB + p * C::KPANEL, &kmap, bar(C::B_KFULL + st), p * 64, kvh,
-                      krow);
-        if (u > 0 && !mbar_wait(bar(C::B_VEMPTY + st), (u - 1) & 1)) {
-          issued = -(it + 1);  // K of this tile issued, V not
-          break;
-        }
-        mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::KB);
-#pragma unroll
-        for (int p = 0; p < C::P; ++p)
-          tma_load_3d(sV + st * C::KB + p * C::KPANEL, &vmap, bar(C::B_VFULL + st), p * 64, kvh,
-                      krow);
-        issued = it + 1;
-        if (*abort_flag) break;
+        for (int p = 0; p < D / 64; ++p)
+          tma_load_3d(sRing + slot * C::TB + p * C::PANEL_T, m, fb, p * 64, head, row);
       }
-      if (issued < n_tiles) {
-        // abandoned: record it and let every copy in flight land before exit
-        raise_err(a.err, kDevErrTimeout);
-        *abort_flag = 1;
-        const int nk = issued < 0 ? -issued : issued;
-        const int nv = issued < 0 ? nk - 1 : issued;
-        mbar_wait(bar(C::B_QFULL), 0, 100000000ull);
-        for (int i = nk - C::NS > 0 ? nk - C::NS : 0; i < nk; ++i)
-          mbar_wait(bar(C::B_KFULL + i % C::NS), (i / C::NS) & 1, 100000000ull);
-        for (int i = nv - C::NS > 0 ? nv - C::NS : 0; i < nv; ++i)
-          mbar_wait(bar(C::B_VFULL + i % C::NS), (i / C::NS) & 1, 100000000ull);
+      __syncwarp();
+      ++issued;
+      if (++slot == C::NSLOT) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      return true;
+    };
+    for (int k = 0; ok && k * G < a.n_units; ++k) {
+      const int u = unit_of(k, cta, G);
+      Unit w;
+      if (u >= a.n_units || !decode_unit(a, u, w)) continue;
+      for (int j = 0; ok && j < w.n_tiles; ++j) {
+        const int row = w.start + (w.t_begin + j) * BN;
+        ok = load_tile(&kmap, row, w.kvh) && load_tile(&vmap, row, w.kvh);
+        if (ok && j == 0) {
+          // the first K/V tiles go out before the Q tiles, which wait for the
+          // previous unit's last QK^T
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (q_loads > 0 && !warp_wait(bar(C::B_QFREE + i), (q_loads - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (leader) {
+              const uint32_t qb = bar(C::B_QFULL + i);
+              mbar_arrive_expect_tx(qb, C::QB);
+#pragma unroll
+              for (int p = 0; p < D / 64; ++p)
+                tma_load_3d(sQ + i * C::QB + p * C::PANEL_Q, &qmap, qb, p * 64, w.h[i],
+                            w.start + w.q0[i]);
+            }
+            __syncwarp();
+          }
+          // counted once both were issued (a half-issued pair is drained below)
+          if (ok) ++q_loads;
+        }
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = umma_idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t idesc_pv = umma_idesc_bf16_f32(BM, D, 0, 1);
-      auto issue_pv = [&](int j) -> bool {
-        const int st = j % C::NS, u = j / C::NS;
-        if (!mbar_wait(bar(C::B_PFULL), j & 1)) return false;
-        if (!mbar_wait(bar(C::B_VFULL + st), u & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P tile, K-major: 16 keys = 32 bytes inside a 128-byte panel row.
-          const uint64_t ad =
-              umma_smem_desc_sw128(sP + (kk >> 2) * C::QPANEL + (kk & 3) * 32, 16, 1024);
-          // B = V tile, MN-major (d contiguous): 16 keys = 16 rows of 128 bytes;
-          // panels of 64 d-columns are KPANEL bytes apart.
-          const uint64_t bd =
-              umma_smem_desc_sw128(sV + st * C::KB + kk * 16 * 128, C::KPANEL, 1024);
-          umma_ss(tmem + C::TM_O, ad, bd, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(C::B_VEMPTY + st));
-        umma_commit(bar(C::B_ODONE));
-        return true;
-      };
-      bool ok = mbar_wait(bar(C::B_QFULL), 0);
-      tc_fence_after();
-      for (int it = 0; ok && it < n_tiles; ++it) {
-        const int st = it % C::NS, u = it / C::NS, sb = it & 1;
-        if (!mbar_wait(bar(C::B_KFULL + st), u & 1)) { ok = false; break; }
-        if (it >= 2 && !mbar_wait(bar(C::B_SFREE + sb), ((it >> 1) - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_q = (kk >> 2) * C::QPANEL + (kk & 3) * 32;
-          const uint32_t off_k = (kk >> 2) * C::KPANEL + (kk & 3) * 32;
-          const uint64_t ad = umma_smem_desc_sw128(sQ + off_q, 16, 1024);
-          const uint64_t bd = umma_smem_desc_sw128(sK + st * C::KB + off_k, 16, 1024);
-          umma_ss(tmem + (sb ? C::TM_S1 : C::TM_S0), ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar(C::B_KEMPTY + st));
-        umma_commit(bar(C::B_SFULL + sb));
-        if (it >= 1) ok = issue_pv(it - 1);
+    // every copy issued must land before the CTA exits
+    if (leader) {
+      const int nring = issued < C::NSLOT ? issued : C::NSLOT;
+      for (int t = 1; t <= nring; ++t) {
+        const int p = issued - t;
+        mbar_wait(bar(C::B_FULL + p % C::NSLOT), (p / C::NSLOT) & 1, kDrainLimitNs);
       }
-      if (ok) ok = issue_pv(n_tiles - 1);
       if (!ok) {
-        raise_err(a.err, kDevErrTimeout);
-        *abort_flag = 1;
+        // the pair of the unit being set up may be partly issued
+        mbar_wait(bar(C::B_QFULL + 0), q_loads & 1, kDrainLimitNs);
       }
-      // every MMA issued above has finished once this commit arrives
-      umma_commit(bar(C::B_DRAIN));
-      mbar_wait(bar(C::B_DRAIN), 0, 100000000ull);
+      if (q_loads > 0) {
+        mbar_wait(bar(C::B_QFULL + 0), (q_loads - 1) & 1, kDrainLimitNs);
+        mbar_wait(bar(C::B_QFULL + 1), (q_loads - 1) & 1, kDrainLimitNs);
+      }
+      if (!ok) raise_err(a.err, kDevErrTimeout);
     }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    // The whole warp runs this loop; tcgen05 instructions are issued by one
+    // elected lane inside each asm block (the same lane every time).
+    constexpr uint32_t idesc_qk = umma_idesc_bf16_f32(BM, BN, 0, 0);
+    constexpr uint32_t idesc_pv = umma_idesc_bf16_f32(BM, D, 0, 1);
+    const uint64_t dq0 = umma_smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t dq1 = umma_smem_desc_sw128(sQ + C::QB, 16, 1024);
+    const uint64_t dk = umma_smem_desc_sw128(sRing, 16, 1024);         // K: K-major
+    const uint64_t dv = umma_smem_desc_sw128(sRing, C::PANEL_T, 1024);  // V: MN-major
+    uint32_t fslot = 0, fphase = 0;  // next ring slot to consume
+    uint32_t rslot = 0;              // next ring slot to release
+    int uc = 0, tc = 0;
+    bool ok = true;
+    auto wait_full = [&](uint32_t& s) -> bool {
+      if (!warp_wait(bar(C::B_FULL + fslot), fphase, abort_flag)) return false;
+      s = fslot;
+      if (++fslot == C::NSLOT) {
+        fslot = 0;
+        fphase ^= 1u;
+      }
+      return true;
+    };
+    auto release = [&]() {
+      umma_commit_elect(bar(C::B_EMPTY + rslot));
+      if (++rslot == C::NSLOT) rslot = 0;
+    };
+    auto commit = [&](int b) { umma_commit_elect(bar(b)); };
+    // S_i = Q_i K^T over d
+    auto qk = [&](int i, uint32_t ks) {
+      const uint64_t kd = dk + ((ks * C::TB) >> 4);
+      const uint32_t d_tm = tmem + static_cast<uint32_t>(i * BN);
+      if constexpr (D == 128)
+        umma_ss_k128_elect(d_tm, i ? dq1 : dq0, kd, idesc_qk);
+      else
+        umma_ss_k64_elect(d_tm, i ? dq1 : dq0, kd, idesc_qk);
+      commit(C::B_SFULL + i);
+    };
+    // O_i (+)= P_i V over the tile's 128 keys
+    auto pv = [&](int i, uint32_t vs, uint32_t acc) {
+      umma_ts_k128_elect(tmem + C::TM_O + static_cast<uint32_t>(i * D),
+                         tmem + static_cast<uint32_t>(i * BN), dv + ((vs * C::TB) >> 4), idesc_pv,
+                         acc);
+    };
+    for (int k = 0; ok && k * G < a.n_units; ++k) {
+      const int u = unit_of(k, cta, G);
+      Unit w;
+      if (u >= a.n_units || !decode_unit(a, u, w)) continue;
+      const int n = w.n_tiles;
+      uint32_t ks = 0, vs = 0;
+      if (!(ok = warp_wait(bar(C::B_QFULL + 0), uc & 1, abort_flag) && wait_full(ks))) break;
+      tc_fence_after();
+      qk(0, ks);
+      if (n == 1) commit(C::B_QFREE + 0);
+      if (!(ok = warp_wait(bar(C::B_QFULL + 1), uc & 1, abort_flag))) break;
+      tc_fence_after();
+      qk(1, ks);
+      release();  // K(0)
+      if (n == 1) commit(C::B_QFREE + 1);
+      for (int j = 0; j < n; ++j, ++tc) {
+        if (!(ok = wait_full(vs) && warp_wait(bar(C::B_PRDY + 0), tc & 1, abort_flag))) break;
+        tc_fence_after();
+        pv(0, vs, j > 0 ? 1u : 0u);
+        if (j == n - 1) commit(C::B_OFULL + 0);
+        if (j + 1 < n) {
+          if (!(ok = wait_full(ks))) break;
+          tc_fence_after();
+          qk(0, ks);
+          if (j + 1 == n - 1) commit(C::B_QFREE + 0);
+        }
+        if (!(ok = warp_wait(bar(C::B_PRDY + 1), tc & 1, abort_flag))) break;
+        tc_fence_after();
+        pv(1, vs, j > 0 ? 1u : 0u);
+        release();  // V(j)
+        if (j == n - 1) commit(C::B_OFULL + 1);
+        if (j + 1 < n) {
+          qk(1, ks);
+          release();  // K(j+1)
+          if (j + 1 == n - 1) commit(C::B_QFREE + 1);
+        }
+      }
+      if (!ok) break;
+      ++uc;
+    }
+    // every MMA issued above has finished once this commit arrives
+    commit(C::B_DRAIN);
+    __syncwarp();
+    mbar_wait(bar(C::B_DRAIN), 0, kDrainLimitNs);
+    if (!ok && lane == 0) raise_err(a.err, kDevErrTimeout);
   } else {
     // ------------------------------------------------ softmax / epilogue
+    const int ti = warp >> 2;              // query tile of this warpgroup
     const int wq = warp & 3;               // TMEM lane quarter of this warp
     const int r = wq * 32 + lane;          // row of the query tile
-    const int i_abs = q0 + r;              // query position in its sequence
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(ti * BN);
+    const uint32_t tO = tmem + lane_off + C::TM_O + static_cast<uint32_t>(ti * D);
     const float sl2 = a.scale_log2;
-    float m = kNegInf, l = 0.f;
+    int uc = 0, tc = 0;
     bool ok = true;
-    for (int it = 0; it < n_tiles; ++it) {
-      const int sb = it & 1;
-      const int kt0 = (t_begin + it) * BN;
-      if (!mbar_wait(bar(C::B_SFULL + sb), (it >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        tmem_ld32(tmem + lane_off + (sb ? C::TM_S1 : C::TM_S0) + 32 * c,
-                  *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_SFREE + sb));
-
-      const bool need_mask = (kt0 + BN > len) || (a.causal && kt0 + BN - 1 > q0) ||
-                             (a.window > 0 && kt0 <= q_last - a.window);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const int j = kt0 + c;
-          const bool vis = j < len && (!a.causal || j <= i_abs) &&
-                           (a.window <= 0 || j > i_abs - a.window);
-          if (!vis) sr[c] = __float_as_uint(kNegInf);
-        }
-      }
-      float mx = kNegInf;
-#pragma unroll
-      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-      const float m_new = fmaxf(m, mx * sl2);
-      const bool resc = m_new > m + kRescaleThreshold;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2(m - m_new);  // 0 when m = -inf
-        m = m_new;
-      }
-      if (it > 0) {
-        // PV of the previous tile must be done before O is touched or P reused
-        if (!mbar_wait(bar(C::B_ODONE), (it - 1) & 1)) { ok = false; break; }
+    for (int k = 0; ok && k * G < a.n_units; ++k) {
+      const int u = unit_of(k, cta, G);
+      Unit w;
+      if (u >= a.n_units || !decode_unit(a, u, w)) continue;
+      const int q0 = w.q0[ti];
+      const int i_abs = q0 + r;  // query position in its sequence
+      float m = kNegInf, l = 0.f;
+      for (int j = 0; j < w.n_tiles; ++j, ++tc) {
+        if (!(ok = warp_wait(bar(C::B_SFULL + ti), tc & 1, abort_flag))) break;
         tc_fence_after();
-        if (__any_sync(0xFFFFFFFFu, resc)) {
+        uint32_t sr[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tmem_wait_ld();
+
+        const int kt0 = (w.t_begin + j) * BN;
+        const bool need_mask = (kt0 + BN > w.len) || (a.causal && kt0 + BN - 1 > q0) ||
+                               (a.window > 0 && kt0 <= q0 + BM - 1 - a.window);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            const int jk = kt0 + c;
+            const bool vis = jk < w.len && (!a.causal || jk <= i_abs) &&
+                             (a.window <= 0 || jk > i_abs - a.window);
+            if (!vis) sr[c] = __float_as_uint(kNegInf);
+          }
+        }
+        // row max: 8 independent chains, three-input max
+        float mx8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float v = fmaxf(__uint_as_float(sr[e]), __uint_as_float(sr[e + 8]));
+#pragma unroll
+          for (int c = 16; c < BN; c += 16)
+            v = fmax3(v, __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
+          mx8[e] = v;
+        }
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
+        const float m_new = fmaxf(m, mx * sl2);
+        const bool resc = m_new > m + kRescaleThreshold;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2(m - m_new);  // 0 when m = -inf
+          m = m_new;
+        }
+        l *= alpha;
+        const float m_use = m == kNegInf ? 0.f : m;
+        // p = 2^(s*scale*log2(e) - m) on pairs of scores: one packed FMA per
+        // pair, one ex2 per score, sums in 8 partials (4 packed accumulators)
+        const uint64_t sl2x2 = f2(sl2, sl2), negm2 = f2(-m_use, -m_use);
+        uint64_t acc2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc2[e] = 0ull;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const uint64_t x = ffma2(f2(__uint_as_float(sr[64 * hf + 2 * e]),
+                                        __uint_as_float(sr[64 * hf + 2 * e + 1])),
+                                     sl2x2, negm2);
+            float x0, x1;
+            unf2(x, x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            acc2[e & 3] = fadd2(acc2[e & 3], f2(p0, p1));
+            pk[e] = pack_bf16(p0, p1);
+          }
+          tmem_st32(tS + 32 * hf, pk);
+        }
+        float ls[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) unf2(acc2[e], ls[2 * e], ls[2 * e + 1]);
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        // O_i is idle here: PV_i(j-1) finished before S_i(j) was signalled and
+        // PV_i(j) waits for this warpgroup's hand-over (the scores are dead by now)
+        if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
-            tmem_ld32(tmem + lane_off + C::TM_O + 32 * c, o);
+            tmem_ld32(tO + 32 * c, o);
             tmem_wait_ld();
+            const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tmem + lane_off + C::TM_O + 32 * c, o);
+            for (int e = 0; e < 32; e += 2) {
+              float lo, hi;
+              unf2(fmul2(f2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
+              o[e] = __float_as_uint(lo);
+              o[e + 1] = __float_as_uint(hi);
+            }
+            tmem_st32(tO + 32 * c, o);
           }
-          tmem_wait_st();
         }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PRDY + ti));
       }
-      l *= alpha;
-      const float m_use = m == kNegInf ? 0.f : m;
-      float lsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = ex2(fmaf(__uint_as_float(sr[8 * c + e]), sl2, -m_use));
-          lsum += p[e];
-        }
-        const uint32_t addr = sP + (c >> 3) * C::QPANEL + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                     "r"(pack_bf16(p[0], p[1])), "r"(pack_bf16(p[2], p[3])),
-                     "r"(pack_bf16(p[4], p[5])), "r"(pack_bf16(p[6], p[7]))
-                     : "memory");
-      }
-      l += lsum;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_PFULL));
-    }
-    if (ok && mbar_wait(bar(C::B_ODONE), (n_tiles - 1) & 1)) {
+      if (!ok) break;
+      if (!(ok = warp_wait(bar(C::B_OFULL + ti), uc & 1, abort_flag))) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int h = w.h[ti];
+      const bool live = i_abs < w.len;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
-                            (static_cast<int64_t>(start + i_abs) * a.Hq + h) * D;
+                            (static_cast<int64_t>(w.start + i_abs) * a.Hq + h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + C::TM_O + 32 * c, o);
+        tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
-        if (r < rows) {
+        if (live) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+          const uint64_t inv2 = f2(inv, inv);
+          uint32_t w[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            dst[v] = w;
+          for (int e = 0; e < 16; ++e) {
+            float lo, hi;
+            unf2(fmul2(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2), lo, hi);
+            w[e] = pack_bf16(lo, hi);
           }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
         }
       }
-      if (a.lse && r < rows)
-        a.lse[static_cast<int64_t>(h) * a.T + start + i_abs] =
+      if (a.lse && live)
+        a.lse[static_cast<int64_t>(h) * a.T + w.start + i_abs] =
             l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
-    } else {
-      raise_err(a.err, kDevErrTimeout);
-      *abort_flag = 1;
+      ++uc;
     }
+    if (!ok && lane == 0) raise_err(a.err, kDevErrTimeout);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -454,19 +626,30 @@ void ensure_pf_attr() {
 
 size_t prefill_bf16_smem(int d) { return d == 128 ? PfCfg<128>::SMEM : PfCfg<64>::SMEM; }
 
-cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& qmap,
-                                const CUtensorMap& kmap, const CUtensorMap& vmap,
+long long prefill_units(int B, int Hq, int Hkv, int max_seqlen, bool* pair_heads) {
+  const long long n_qt = (max_seqlen + BM - 1) / BM;
+  const bool pair = ((Hq / Hkv) % 2) == 0;
+  if (pair_heads) *pair_heads = pair;
+  return pair ? n_qt * (Hq / 2) * B : ((n_qt + 1) / 2) * Hq * static_cast<long long>(B);
+}
+
+cudaError_t launch_prefill_bf16(const PrefillArgs& a0, const CUtensorMap& qmap,
+                                const CUtensorMap& kmap, const CUtensorMap& vmap, int num_sms,
                                 cudaStream_t s) {
-  const int n_qt = (a.max_seqlen + BM - 1) / BM;
-  const long long grid = static_cast<long long>(n_qt) * a.Hq * a.B;
-  if (grid == 0) return cudaSuccess;
-  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  PrefillArgs a = a0;
+  bool pair = false;
+  const long long units = prefill_units(a.B, a.Hq, a.Hkv, a.max_seqlen, &pair);
+  if (units == 0) return cudaSuccess;
+  if (units > INT_MAX) return cudaErrorInvalidConfiguration;
+  a.pair_heads = pair ? 1 : 0;
+  a.n_units = static_cast<int>(units);
+  const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
   if (a.d == 128) {
     ensure_pf_attr<128>();
-    prefill_bf16_kernel<128><<<static_cast<unsigned>(grid), 192, PfCfg<128>::SMEM, s>>>(qmap, kmap, vmap, a);
+    prefill_bf16_kernel<128><<<grid, kThreads, PfCfg<128>::SMEM, s>>>(qmap, kmap, vmap, a);
   } else {
     ensure_pf_attr<64>();
-    prefill_bf16_kernel<64><<<static_cast<unsigned>(grid), 192, PfCfg<64>::SMEM, s>>>(qmap, kmap, vmap, a);
+    prefill_bf16_kernel<64><<<grid, kThreads, PfCfg<64>::SMEM, s>>>(qmap, kmap, vmap, a);
   }
   return cudaGetLastError();
 }

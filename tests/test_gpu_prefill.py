@@ -37,6 +37,19 @@ def test_prefill_bf16_varlen(d, hq, hkv, causal):
     assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
 
 
+@pytest.mark.parametrize("hq,hkv,window", [(8, 2, 0), (6, 2, 0), (3, 3, 300)])
+def test_prefill_bf16_many_units_per_cta(hq, hkv, window):
+    """More work units than SMs, so each persistent CTA runs several units back
+    to back (ring slots, Q buffers and TMEM reused across units). (8, 2) pairs
+    two heads per unit; (6, 2) and (3, 3) have an odd group size and pair two
+    row tiles of one head instead."""
+    lengths = [700, 1500, 260, 2000, 129]
+    o, lse, want_o, want_lse = run_varlen(lengths, hq, hkv, 128, torch.bfloat16, causal=True,
+                                          window=window, seed=hq * 10 + hkv)
+    assert_close_bf16(o, want_o, "o")
+    assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
+
+
 @pytest.mark.parametrize("window", [1, 64, 128, 200])
 def test_prefill_bf16_window(window):
     o, lse, want_o, want_lse = run_varlen([50, 400, 700], 8, 2, 128, torch.bfloat16,
