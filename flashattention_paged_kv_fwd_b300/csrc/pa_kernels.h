@@ -67,6 +67,7 @@ struct PrefillArgs {
   float scale_log2;
   int pair_heads;  // bf16 path: a work unit pairs two query heads (else two row tiles)
   int n_units;     // bf16 path: work units in the launch
+  int compact;     // bf16 path: build the sorted on-chip work list (packed sequences)
 };
 
 // Work units of the bf16 prefill (two 128-row query tiles each).

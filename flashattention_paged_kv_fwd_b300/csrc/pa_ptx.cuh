@@ -349,6 +349,7 @@ enum : int32_t {
   kDevErrBadBlock = 1,     // a block-table entry outside [0, num_blocks)
   kDevErrBadPosition = 2,  // a token position beyond the sequence's table
   kDevErrTimeout = 4,      // a bounded wait gave up
+  kDevErrInternal = 8,     // unusable launch state (misaligned shared memory)
 };
 
 __device__ __forceinline__ void raise_err(int32_t* flag, int32_t bits) {

@@ -69,6 +69,8 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows > 256x
 
+constexpr int kMaxSchedSeqs = 512;  // packed sequences the on-chip work list can sort
+
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;  // 8 softmax warps + producer + MMA issuer
@@ -93,7 +95,8 @@ struct PfCfg {
   static constexpr int B_OFULL = 8 + 2 * NSLOT;   // + query tile
   static constexpr int B_DRAIN = 10 + 2 * NSLOT;
   static constexpr int NBAR = 11 + 2 * NSLOT;
-  static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
+  static constexpr int OFF_SCHED = OFF_BAR + NBAR * 8 + 16;  // after the TMEM slot + abort flag
+  static constexpr int SMEM = OFF_SCHED + 2 * kMaxSchedSeqs * 2 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_O = 2 * BN;     // S_i at i*BN, O_i at TM_O + i*D
 };
@@ -111,31 +114,25 @@ struct Unit {
   int n_tiles;     // key tiles streamed
 };
 
-__device__ __forceinline__ bool decode_unit(const PrefillArgs& a, int u, Unit& w) {
-  const int n_qt = (a.max_seqlen + BM - 1) / BM;
-  int qt0, qt1, b;
+// Work list. Level L of a sequence is its L-th 128-row query tile (two-head
+// units) or its L-th pair of query tiles (two-tile units); under a causal mask
+// a higher level has a longer key range. Units are ordered by level, highest
+// first, then by `pair` (head pair, or head) and sequence.
+__device__ __forceinline__ bool decode_unit(const PrefillArgs& a, int level, int b, int pair,
+                                            Unit& w) {
+  int qt0, qt1;
   if (a.pair_heads) {
-    const int per = (a.Hq >> 1) * a.B;
-    const int lvl = u / per, rem = u - lvl * per;
-    b = rem % a.B;
-    const int hp = rem / a.B;
-    qt0 = qt1 = a.causal ? n_qt - 1 - lvl : lvl;
-    w.h[0] = 2 * hp;
-    w.h[1] = 2 * hp + 1;
+    qt0 = qt1 = level;
+    w.h[0] = 2 * pair;
+    w.h[1] = 2 * pair + 1;
   } else {
-    const int n_qp = (n_qt + 1) >> 1;
-    const int per = a.Hq * a.B;
-    const int lvl = u / per, rem = u - lvl * per;
-    b = rem % a.B;
-    const int h = rem / a.B;
-    const int qp = a.causal ? n_qp - 1 - lvl : lvl;
-    qt0 = 2 * qp;
+    qt0 = 2 * level;
     qt1 = qt0 + 1;
-    w.h[0] = w.h[1] = h;
+    w.h[0] = w.h[1] = pair;
   }
   if (a.cu_seqlens) {
     w.start = a.cu_seqlens[b];
-    w.len = a.cu_seqlens[b + 1] - w.start;
+    w.len = min(a.cu_seqlens[b + 1] - w.start, a.max_seqlen);
   } else {
     w.start = b * a.N;
     w.len = a.N;
@@ -151,6 +148,57 @@ __device__ __forceinline__ bool decode_unit(const PrefillArgs& a, int u, Unit& w
   w.kvh = w.h[0] / (a.Hq / a.Hkv);
   return true;
 }
+
+// Index -> (level, sequence, pair) over the work list. Without a compact
+// list (fixed-length batches, or more packed sequences than the on-chip
+// table holds) every (level, pair, sequence) of the longest sequence is an
+// index and indices past a shorter sequence's end are skipped. With it
+// (packed batches), sequences are sorted by their level count, longest first,
+// and only existing units get an index, so consecutive indices -- handed out
+// round-robin to the CTAs -- are all real work.
+struct Sched {
+  const uint16_t* order;  // sequence of each rank
+  const uint16_t* nl;     // levels of each rank, non-increasing
+  int nseq, npairs, nlev;
+  bool compact;
+  int L, cum, cnt;        // compact walk: current level, indices below it, ranks that have it
+
+  __device__ __forceinline__ int count_gt(int lv) const {  // ranks with more than lv levels
+    int lo = 0, hi = nseq;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (nl[mid] > lv) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+  }
+  __device__ __forceinline__ void start() {
+    if (compact) {
+      L = static_cast<int>(nl[0]) - 1;
+      cum = 0;
+      cnt = L >= 0 ? count_gt(L) : 0;
+    }
+  }
+  // indices must be visited in increasing order
+  __device__ __forceinline__ void map(int v, int& level, int& b, int& pair) {
+    if (compact) {
+      while (v >= cum + cnt * npairs) {
+        cum += cnt * npairs;
+        --L;
+        cnt = count_gt(L);
+      }
+      const int j = v - cum;
+      b = order[j % cnt];
+      pair = j / cnt;
+      level = L;
+    } else {
+      const int per = npairs * nseq;
+      const int lvl = v / per, rem = v - lvl * per;
+      b = rem % nseq;
+      pair = rem / nseq;
+      level = nlev - 1 - lvl;
+    }
+  }
+};
 
 // Unit of the k-th round of CTA c: rounds alternate direction ("snake"), so
 // with units sorted heaviest first every CTA gets a similar total.
@@ -194,15 +242,50 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
 
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gb = smem_raw + (base - raw);
+  // 1024-byte alignment is what the 128-byte swizzle expects of every tile
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_u32(smem_raw);
+  if (base & 1023u) {
+    if (threadIdx.x == 0) raise_err(a.err, kDevErrInternal);
+    return;
+  }
+  uint8_t* gb = smem_raw;
   const uint32_t sQ = base + C::OFF_Q, sRing = base + C::OFF_RING;
   const uint32_t bar0 = base + C::OFF_BAR;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  // ---- work list (all threads): sort packed sequences by level count
+  uint16_t* s_order = reinterpret_cast<uint16_t*>(gb + C::OFF_SCHED);
+  uint16_t* s_nl = s_order + kMaxSchedSeqs;
+  int* s_total = reinterpret_cast<int*>(s_nl + kMaxSchedSeqs);
+  const int npairs = a.pair_heads ? (a.Hq >> 1) : a.Hq;
+  if (a.compact) {
+    uint16_t* tmp = reinterpret_cast<uint16_t*>(gb + C::OFF_RING);  // the ring is still unused
+    if (threadIdx.x == 0) *s_total = 0;
+    for (int b = threadIdx.x; b < a.B; b += kThreads) {
+      const int len = max(0, min(a.cu_seqlens[b + 1] - a.cu_seqlens[b], a.max_seqlen));
+      const int nqt = (len + BM - 1) / BM;
+      tmp[b] = static_cast<uint16_t>(a.pair_heads ? nqt : (nqt + 1) >> 1);
+    }
+    __syncthreads();
+    int part = 0;
+    for (int b = threadIdx.x; b < a.B; b += kThreads) {
+      const int n = tmp[b];
+      int rank = 0;
+      for (int b2 = 0; b2 < a.B; ++b2) {
+        const int n2 = tmp[b2];
+        rank += (n2 > n) || (n2 == n && b2 < b);
+      }
+      s_order[rank] = static_cast<uint16_t>(b);
+      s_nl[rank] = static_cast<uint16_t>(n);
+      part += n;
+    }
+    __syncthreads();  // *s_total zeroed and every rank of tmp read
+    if (part) atomicAdd(s_total, part * npairs);
+    fence_proxy_async_smem();  // the ring's generic writes before TMA reuses it
+  }
 
   if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -229,6 +312,15 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  Sched sched;
+  sched.order = s_order;
+  sched.nl = s_nl;
+  sched.nseq = a.B;
+  sched.npairs = npairs;
+  sched.nlev = a.pair_heads ? (a.max_seqlen + BM - 1) / BM : ((a.max_seqlen + BM - 1) / BM + 1) / 2;
+  sched.compact = a.compact != 0;
+  sched.start();
+  const int n_units = a.compact ? *s_total : a.n_units;
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
@@ -260,10 +352,13 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       return true;
     };
-    for (int k = 0; ok && k * G < a.n_units; ++k) {
+    for (int k = 0; ok && k * G < n_units; ++k) {
       const int u = unit_of(k, cta, G);
       Unit w;
-      if (u >= a.n_units || !decode_unit(a, u, w)) continue;
+      int lv, sb, pr;
+      if (u >= n_units) continue;
+      sched.map(u, lv, sb, pr);
+      if (!decode_unit(a, lv, sb, pr, w)) continue;
       for (int j = 0; ok && j < w.n_tiles; ++j) {
         const int row = w.start + (w.t_begin + j) * BN;
         ok = load_tile(&kmap, row, w.kvh) && load_tile(&vmap, row, w.kvh);
@@ -351,10 +446,13 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
                          tmem + static_cast<uint32_t>(i * BN), dv + ((vs * C::TB) >> 4), idesc_pv,
                          acc);
     };
-    for (int k = 0; ok && k * G < a.n_units; ++k) {
+    for (int k = 0; ok && k * G < n_units; ++k) {
       const int u = unit_of(k, cta, G);
       Unit w;
-      if (u >= a.n_units || !decode_unit(a, u, w)) continue;
+      int lv, sb, pr;
+      if (u >= n_units) continue;
+      sched.map(u, lv, sb, pr);
+      if (!decode_unit(a, lv, sb, pr, w)) continue;
       const int n = w.n_tiles;
       uint32_t ks = 0, vs = 0;
       if (!(ok = warp_wait(bar(C::B_QFULL + 0), uc & 1, abort_flag) && wait_full(ks))) break;
@@ -407,10 +505,13 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
     const float sl2 = a.scale_log2;
     int uc = 0, tc = 0;
     bool ok = true;
-    for (int k = 0; ok && k * G < a.n_units; ++k) {
+    for (int k = 0; ok && k * G < n_units; ++k) {
       const int u = unit_of(k, cta, G);
       Unit w;
-      if (u >= a.n_units || !decode_unit(a, u, w)) continue;
+      int lv, sb, pr;
+      if (u >= n_units) continue;
+      sched.map(u, lv, sb, pr);
+      if (!decode_unit(a, lv, sb, pr, w)) continue;
       const int q0 = w.q0[ti];
       const int i_abs = q0 + r;  // query position in its sequence
       float m = kNegInf, l = 0.f;
@@ -643,6 +744,7 @@ cudaError_t launch_prefill_bf16(const PrefillArgs& a0, const CUtensorMap& qmap,
   if (units > INT_MAX) return cudaErrorInvalidConfiguration;
   a.pair_heads = pair ? 1 : 0;
   a.n_units = static_cast<int>(units);
+  a.compact = (a.cu_seqlens && a.B <= kMaxSchedSeqs && (a.max_seqlen + BM - 1) / BM <= 65535) ? 1 : 0;
   const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
   if (a.d == 128) {
     ensure_pf_attr<128>();

@@ -72,7 +72,13 @@ enum {
   PA_ERR_WORKSPACE = 4    /* workspace missing or smaller than required */
 };
 
-enum { PA_DEV_BAD_BLOCK = 1, PA_DEV_BAD_POSITION = 2, PA_DEV_TIMEOUT = 4 };
+enum {
+  PA_DEV_BAD_BLOCK = 1,    /* a block-table entry outside [0, num_blocks) */
+  PA_DEV_BAD_POSITION = 2, /* a token position beyond the sequence's table */
+  PA_DEV_TIMEOUT = 4,      /* a bounded wait gave up */
+  PA_DEV_INTERNAL = 8      /* a kernel found its launch state unusable (e.g. a misaligned
+                              shared-memory base); it computed nothing */
+};
 
 /* Short description of a status code (static string). */
 PA_API const char* pa_status_str(int status);
