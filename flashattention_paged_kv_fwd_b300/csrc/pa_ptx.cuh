@@ -303,11 +303,11 @@ __device__ __forceinline__ void umma_ss_k64_elect(uint32_t d, uint64_t a, uint64
       "l"(a), "l"(b), "r"(idesc)
       : "memory");
 }
-// O (+)= P V over 128 keys: P is read from TMEM (8 columns per 16 keys), V's
-// 16-row k-steps are 2 KB apart (128 descriptor units). `acc` = 0 makes the
-// first step overwrite O.
-__device__ __forceinline__ void umma_ts_k128_elect(uint32_t d, uint32_t p, uint64_t b,
-                                                   uint32_t idesc, uint32_t acc) {
+// O (+)= P V over 64 keys (four 16-key steps): P is read from TMEM (8
+// columns per 16 keys), V's 16-row k-steps are 2 KB apart (128 descriptor
+// units). `acc` = 0 makes the first step overwrite O.
+__device__ __forceinline__ void umma_ts_k64keys_elect(uint32_t d, uint32_t p, uint64_t b,
+                                                      uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred P, A;\n\t.reg .b64 b1;\n\t.reg .b32 p1;\n\t"
       "elect.sync _|P, 0xffffffff;\n\t"
@@ -318,14 +318,6 @@ __device__ __forceinline__ void umma_ts_k128_elect(uint32_t d, uint32_t p, uint6
       "add.s32 p1, %1, 16;\n\tadd.s64 b1, %2, 256;\n\t"
       "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
       "add.s32 p1, %1, 24;\n\tadd.s64 b1, %2, 384;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
-      "add.s32 p1, %1, 32;\n\tadd.s64 b1, %2, 512;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
-      "add.s32 p1, %1, 40;\n\tadd.s64 b1, %2, 640;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
-      "add.s32 p1, %1, 48;\n\tadd.s64 b1, %2, 768;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
-      "add.s32 p1, %1, 56;\n\tadd.s64 b1, %2, 896;\n\t"
       "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [p1], b1, %3, 1;\n\t"
       "}" ::"r"(d),
       "r"(p), "l"(b), "r"(idesc), "r"(acc)

@@ -91,10 +91,10 @@ struct PfCfg {
   static constexpr int B_FULL = 4;             // + ring slot
   static constexpr int B_EMPTY = 4 + NSLOT;    // + ring slot
   static constexpr int B_SFULL = 4 + 2 * NSLOT;   // + query tile
-  static constexpr int B_PRDY = 6 + 2 * NSLOT;    // + query tile
-  static constexpr int B_OFULL = 8 + 2 * NSLOT;   // + query tile
-  static constexpr int B_DRAIN = 10 + 2 * NSLOT;
-  static constexpr int NBAR = 11 + 2 * NSLOT;
+  static constexpr int B_PRDY = 6 + 2 * NSLOT;    // + 2 * query tile + half (keys 0-63 / 64-127)
+  static constexpr int B_OFULL = 10 + 2 * NSLOT;  // + query tile
+  static constexpr int B_DRAIN = 12 + 2 * NSLOT;
+  static constexpr int NBAR = 13 + 2 * NSLOT;
   static constexpr int OFF_SCHED = OFF_BAR + NBAR * 8 + 16;  // after the TMEM slot + abort flag
   static constexpr int SMEM = OFF_SCHED + 2 * kMaxSchedSeqs * 2 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -293,7 +293,8 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         mbar_init(bar(C::B_QFULL + i), 1);
         mbar_init(bar(C::B_QFREE + i), 1);
         mbar_init(bar(C::B_SFULL + i), 1);
-        mbar_init(bar(C::B_PRDY + i), 128);
+        mbar_init(bar(C::B_PRDY + 2 * i), 128);
+        mbar_init(bar(C::B_PRDY + 2 * i + 1), 128);
         mbar_init(bar(C::B_OFULL + i), 1);
       }
       for (int s = 0; s < C::NSLOT; ++s) {
@@ -440,11 +441,19 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         umma_ss_k64_elect(d_tm, i ? dq1 : dq0, kd, idesc_qk);
       commit(C::B_SFULL + i);
     };
-    // O_i (+)= P_i V over the tile's 128 keys
-    auto pv = [&](int i, uint32_t vs, uint32_t acc) {
-      umma_ts_k128_elect(tmem + C::TM_O + static_cast<uint32_t>(i * D),
-                         tmem + static_cast<uint32_t>(i * BN), dv + ((vs * C::TB) >> 4), idesc_pv,
-                         acc);
+    // O_i (+)= P_i V over the tile's 128 keys, in two halves of 64 keys: each
+    // half is issued as soon as the softmax has handed over its part of P
+    auto pv = [&](int i, uint32_t vs, uint32_t acc) -> bool {
+      const uint32_t o_tm = tmem + C::TM_O + static_cast<uint32_t>(i * D);
+      const uint32_t p_tm = tmem + static_cast<uint32_t>(i * BN);
+      const uint64_t vd = dv + ((vs * C::TB) >> 4);
+      if (!warp_wait(bar(C::B_PRDY + 2 * i), tc & 1, abort_flag)) return false;
+      tc_fence_after();
+      umma_ts_k64keys_elect(o_tm, p_tm, vd, idesc_pv, acc);
+      if (!warp_wait(bar(C::B_PRDY + 2 * i + 1), tc & 1, abort_flag)) return false;
+      tc_fence_after();
+      umma_ts_k64keys_elect(o_tm, p_tm + 32, vd + 512, idesc_pv, 1u);
+      return true;
     };
     for (int k = 0; ok && k * G < n_units; ++k) {
       const int u = unit_of(k, cta, G);
@@ -465,9 +474,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       release();  // K(0)
       if (n == 1) commit(C::B_QFREE + 1);
       for (int j = 0; j < n; ++j, ++tc) {
-        if (!(ok = wait_full(vs) && warp_wait(bar(C::B_PRDY + 0), tc & 1, abort_flag))) break;
-        tc_fence_after();
-        pv(0, vs, j > 0 ? 1u : 0u);
+        if (!(ok = wait_full(vs) && pv(0, vs, j > 0 ? 1u : 0u))) break;
         if (j == n - 1) commit(C::B_OFULL + 0);
         if (j + 1 < n) {
           if (!(ok = wait_full(ks))) break;
@@ -475,9 +482,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
           qk(0, ks);
           if (j + 1 == n - 1) commit(C::B_QFREE + 0);
         }
-        if (!(ok = warp_wait(bar(C::B_PRDY + 1), tc & 1, abort_flag))) break;
-        tc_fence_after();
-        pv(1, vs, j > 0 ? 1u : 0u);
+        if (!(ok = pv(1, vs, j > 0 ? 1u : 0u))) break;
         release();  // V(j)
         if (j == n - 1) commit(C::B_OFULL + 1);
         if (j + 1 < n) {
@@ -558,7 +563,9 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         l *= alpha;
         const float m_use = m == kNegInf ? 0.f : m;
         // p = 2^(s*scale*log2(e) - m) on pairs of scores: one packed FMA per
-        // pair, one ex2 per score, sums in 8 partials (4 packed accumulators)
+        // pair, one ex2 per score, sums in 8 partials (4 packed accumulators).
+        // P goes to TMEM and is handed to the MMA warp in two halves of 64
+        // keys, so the first half of PV runs while the second is computed.
         const uint64_t sl2x2 = f2(sl2, sl2), negm2 = f2(-m_use, -m_use);
         uint64_t acc2[4];
 #pragma unroll
@@ -578,33 +585,33 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
             pk[e] = pack_bf16(p0, p1);
           }
           tmem_st32(tS + 32 * hf, pk);
+          if (hf == 0 && j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
+            // O_i is idle here: PV_i(j-1) finished before S_i(j) was signalled
+            // and PV_i(j) waits for the first hand-over below
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + 32 * c, o);
+              tmem_wait_ld();
+              const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float lo, hi;
+                unf2(fmul2(f2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
+                o[e] = __float_as_uint(lo);
+                o[e + 1] = __float_as_uint(hi);
+              }
+              tmem_st32(tO + 32 * c, o);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar(C::B_PRDY + 2 * ti + hf));
         }
         float ls[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) unf2(acc2[e], ls[2 * e], ls[2 * e + 1]);
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-        // O_i is idle here: PV_i(j-1) finished before S_i(j) was signalled and
-        // PV_i(j) waits for this warpgroup's hand-over (the scores are dead by now)
-        if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32 * c, o);
-            tmem_wait_ld();
-            const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float lo, hi;
-              unf2(fmul2(f2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
-              o[e] = __float_as_uint(lo);
-              o[e + 1] = __float_as_uint(hi);
-            }
-            tmem_st32(tO + 32 * c, o);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_PRDY + ti));
       }
       if (!ok) break;
       if (!(ok = warp_wait(bar(C::B_OFULL + ti), uc & 1, abort_flag))) break;
