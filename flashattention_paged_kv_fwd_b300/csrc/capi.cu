@@ -71,17 +71,23 @@ bool encode_3d(CUtensorMap* m, const void* ptr, int d, int heads, long long rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Pool [num_blocks, block_size, heads, d] described with the dimensions in
+// the order (d, token, head, block): one box of 64 elements x block_size
+// tokens x `box_heads` heads lands in shared memory as `box_heads` head tiles
+// of block_size x 128 bytes, each 128-byte swizzled exactly like a one-head
+// box, so a whole page of a CTA's heads is one copy per 64-column panel.
 bool encode_pool(CUtensorMap* m, const void* ptr, int d, int heads, int block_size,
-                 int num_blocks) {
+                 int num_blocks, int box_heads) {
   EncodeFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
-                              static_cast<cuuint64_t>(block_size),
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(block_size),
+                              static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(heads) * d * 2,
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(heads) * d * 2,
+                                 static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(block_size) * heads * d * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(block_size), 1};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(block_size),
+                             static_cast<cuuint32_t>(box_heads), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -230,8 +236,8 @@ int pa_attn_decode_paged(const void* q, const void* k_cache, const void* v_cache
     e = pa::launch_decode_f32(a, p, s);
   } else {
     CUtensorMap km, vm;
-    if (!encode_pool(&km, k_cache, d, Hkv, block_size, num_blocks) ||
-        !encode_pool(&vm, v_cache, d, Hkv, block_size, num_blocks))
+    if (!encode_pool(&km, k_cache, d, Hkv, block_size, num_blocks, p.hg) ||
+        !encode_pool(&vm, v_cache, d, Hkv, block_size, num_blocks, p.hg))
       return PA_ERR_CUDA;
     e = pa::launch_decode_bf16(a, p, km, vm, s);
   }

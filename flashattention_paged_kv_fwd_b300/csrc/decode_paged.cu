@@ -15,9 +15,13 @@
 //  * CTA = (sequence, group of `hg` KV heads, range of `chunk` blocks).
 //  * One producer thread walks the range's slice of the block table (staged
 //    in shared memory) and issues TMA copies of each block's K and V rows for
-//    the CTA's heads into a ring of `stages` shared-memory buffers. Each copy
-//    is one (head, 64-element panel) box of 16 tokens x 128 B, 128-byte
-//    swizzled so that the ldmatrix reads below are bank-conflict free.
+//    the CTA's heads into a ring of `stages` shared-memory buffers. One copy
+//    per 64-element panel brings the page's rows of all the CTA's heads
+//    (16 tokens x hg heads x 128 B, up to 24 KB): the pool's tensor map lists
+//    its dimensions as (d, token, head, block), so the box lands as hg head
+//    tiles of 16 tokens x 128 B, each 128-byte swizzled so that the ldmatrix
+//    reads below are bank-conflict free. (Per-head 2 KB copies cap an SM near
+//    40 GB/s: copies, not bytes, were the limit.)
 //  * One consumer warp per (KV head, 16 query heads): the G = Hq/Hkv query
 //    heads that share the KV head are packed as the 16 rows of an m16n8k16
 //    warp MMA (rows past G are zero), so K and V are read from shared memory
@@ -71,6 +75,11 @@ __device__ __forceinline__ SeqRange seq_range(int len, int max_blocks, int windo
 // accumulators (d/8 x 4 fp32) and Q fragments stay in registers.
 template <int D>
 constexpr int kMaxConsumerWarps = D == 128 ? 8 : 12;
+// Planner inputs: registers per thread of the two instantiations (ptxas -v,
+// rounded up to the allocation step) and shared memory per SM.
+constexpr int kRegsD128 = 168;
+constexpr int kRegsD64 = 120;
+constexpr int kSmemPerSm = 228 * 1024;
 
 template <int D>
 __global__ void __launch_bounds__((kMaxConsumerWarps<D> + 1) * 32, 1)
@@ -146,13 +155,12 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
         if (ok) {
           mbar_arrive_expect_tx(full(st), stage_bytes);
           const uint32_t sb = base + st * stage_bytes;
-          for (int g = 0; g < hg; ++g) {
-            const int head = hc * hg + g;
+          // one copy per 64-column panel brings the page's rows of all hg
+          // heads: tiles [panel][head] of 16 tokens x 128 B, K then V
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-              tma_load_4d(sb + (g * P + p) * kBox, &kmap, full(st), p * 64, head, 0, phys);
-              tma_load_4d(sb + ((hg + g) * P + p) * kBox, &vmap, full(st), p * 64, head, 0, phys);
-            }
+          for (int p = 0; p < P; ++p) {
+            tma_load_4d(sb + p * hg * kBox, &kmap, full(st), p * 64, 0, hc * hg, phys);
+            tma_load_4d(sb + (P + p) * hg * kBox, &vmap, full(st), p * 64, 0, hc * hg, phys);
           }
           valid_mask |= 1u << st;
         } else {
@@ -211,8 +219,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     const int phys = phys_s[st];
     if (phys >= 0) {
-      const uint32_t kb = base + st * stage_bytes + g * P * kBox;
-      const uint32_t vb = base + st * stage_bytes + (hg + g) * P * kBox;
+      const uint32_t kb = base + st * stage_bytes + g * kBox;           // panel p at + p*hg*kBox
+      const uint32_t vb = base + st * stage_bytes + (P * hg + g) * kBox;
       const int tok0 = (pstart + i) * kBlk;
 
       float sc[2][4];
@@ -221,7 +229,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const int c = kk * 2 + (mi & 1);
-        const uint32_t addr = kb + (c >> 3) * kBox + ktok * 128 + (((c & 7) ^ (ktok & 7)) << 4);
+        const uint32_t addr = kb + (c >> 3) * hg * kBox + ktok * 128 + (((c & 7) ^ (ktok & 7)) << 4);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(addr, b0, b1, b2, b3);
         mma_bf16_16816(sc[0], qa[kk], b0, b1);
@@ -279,7 +287,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
       for (int jj = 0; jj < D / 16; ++jj) {
         const int c = jj * 2 + (mi >> 1);
-        const uint32_t addr = vb + (c >> 3) * kBox + vtok * 128 + (((c & 7) ^ (vtok & 7)) << 4);
+        const uint32_t addr = vb + (c >> 3) * hg * kBox + vtok * 128 + (((c & 7) ^ (vtok & 7)) << 4);
         uint32_t v0, v1, v2, v3;
         ldsm_x4_t(addr, v0, v1, v2, v3);
         mma_bf16_16816(acc[2 * jj], pa, v0 & mlo, v1 & mhi);
@@ -401,6 +409,10 @@ decode_f32_kernel(const DecodeArgs a, const int chunk, const int num_splits) {
 template <typename OutT, int D>
 __global__ void __launch_bounds__(256)
 decode_merge_kernel(const DecodeArgs a, const int chunk, const int num_splits) {
+  // launched as a programmatic dependent of the decode kernel: its CTAs may
+  // start while the decode's last CTAs finish, and wait here until that grid
+  // has completed and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int idx = blockIdx.x * 8 + warp;
   if (idx >= a.B * a.Hq) return;
@@ -412,25 +424,55 @@ decode_merge_kernel(const DecodeArgs a, const int chunk, const int num_splits) {
   for (int i = lane; i < r.n_split; i += 32) mx = fmaxf(mx, ls[i]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-  float acc[D / 32];
+  // each lane owns D/32 consecutive columns; four ranges are loaded before
+  // any is used, so their latencies overlap
+  constexpr int V = D / 32;
+  float acc[V];
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) acc[c] = 0.f;
+  for (int c = 0; c < V; ++c) acc[c] = 0.f;
   float total = 0.f;
-  const float* wo = a.ws_o + static_cast<int64_t>(idx) * num_splits * D;
-  for (int i = 0; i < r.n_split; ++i) {
+  const float* wo = a.ws_o + static_cast<int64_t>(idx) * num_splits * D + lane * V;
+  auto load_row = [&](int i, float (&v)[V]) {
+    if constexpr (V == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(wo + static_cast<int64_t>(i) * D);
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(wo + static_cast<int64_t>(i) * D);
+      v[0] = t.x; v[1] = t.y;
+    }
+  };
+  int i = 0;
+  for (; i + 4 <= r.n_split; i += 4) {
+    float v[4][V], lw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      lw[u] = ls[i + u];
+      load_row(i + u, v[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = expf(lw[u] - mx);
+      total += w;
+#pragma unroll
+      for (int c = 0; c < V; ++c) acc[c] = fmaf(w, v[u][c], acc[c]);
+    }
+  }
+  for (; i < r.n_split; ++i) {
+    float v[V];
+    load_row(i, v);
     const float w = expf(ls[i] - mx);
     total += w;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(w, wo[i * D + lane + 32 * c], acc[c]);
+    for (int c = 0; c < V; ++c) acc[c] = fmaf(w, v[c], acc[c]);
   }
   const float inv = 1.f / total;
-  OutT* o = static_cast<OutT*>(a.o) + static_cast<int64_t>(idx) * D;
+  OutT* o = static_cast<OutT*>(a.o) + static_cast<int64_t>(idx) * D + lane * V;
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
+  for (int c = 0; c < V; ++c) {
     if constexpr (sizeof(OutT) == 2)
-      o[lane + 32 * c] = __float2bfloat16_rn(acc[c] * inv);
+      o[c] = __float2bfloat16_rn(acc[c] * inv);
     else
-      o[lane + 32 * c] = acc[c] * inv;
+      o[c] = acc[c] * inv;
   }
   if (lane == 0 && a.lse) a.lse[h * a.B + b] = mx + logf(total);
 }
@@ -455,6 +497,7 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
                        int num_splits_req, int sm_count, bool f32) {
   DecodePlan p{};
   const int G = Hq / Hkv;
+  const int sms = sm_count > 0 ? sm_count : 148;
   int eff = max_blocks;  // blocks one sequence can touch
   if (window > 0) {
     const int wb = (window + block_size - 2) / block_size + 1;
@@ -485,11 +528,31 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
   if (num_splits_req > 0) {
     chunk = (eff + num_splits_req - 1) / num_splits_req;
   } else {
+    // Ranges of 4-64 blocks, about two CTAs per SM: fine enough to even out
+    // sequences of very different lengths.
     const long long units = static_cast<long long>(B) * p.head_chunks;
-    const long long target = 2LL * (sm_count > 0 ? sm_count : 148);
+    const long long target = 2LL * sms;
     long long c = (units * eff + target - 1) / target;
     c = c < 4 ? 4 : (c > 64 ? 64 : c);
     chunk = static_cast<int>(c);
+    // A small call that this cut would spread over a few waves (a ring CTA
+    // holds most of an SM's shared memory and registers) runs in one wave
+    // instead: the largest range count per sequence that still fits.
+    if (!f32) {
+      const int regs = d == 128 ? kRegsD128 : kRegsD64;
+      const int P = d / 64;
+      const long long smem = 1024 + p.stages * (2LL * p.hg * P * kBox) + 64;
+      long long cps = kSmemPerSm / (smem + 1024);
+      const long long cps_regs = 65536 / (static_cast<long long>(p.threads) * regs);
+      cps = cps < cps_regs ? cps : cps_regs;
+      if (cps < 1) cps = 1;
+      const long long slots = cps * sms;
+      const long long ctas = units * ((eff + chunk - 1) / chunk);
+      if (ctas > slots && ctas <= 3 * slots && units <= slots) {
+        const long long splits = slots / units;
+        chunk = static_cast<int>((eff + splits - 1) / splits);
+      }
+    }
   }
   if (chunk > eff) chunk = eff;
   if (chunk < 1) chunk = 1;
@@ -510,6 +573,24 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
   return p;
 }
 
+// The merge kernel follows the decode kernel on the same stream as a
+// programmatic dependent launch, which hides its launch latency behind the
+// decode's tail.
+template <typename K>
+cudaError_t launch_merge(K kernel, const DecodeArgs& a, const DecodePlan& p, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.B * a.Hq + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, p.chunk, p.num_splits);
+}
+
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodePlan& p, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t s) {
   const dim3 grid(p.num_splits, p.head_chunks, a.B);
@@ -524,12 +605,8 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodePlan& p, const C
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.num_splits <= 1) return e;
-  const int mblocks = (a.B * a.Hq + 7) / 8;
-  if (a.d == 128)
-    decode_merge_kernel<__nv_bfloat16, 128><<<mblocks, 256, 0, s>>>(a, p.chunk, p.num_splits);
-  else
-    decode_merge_kernel<__nv_bfloat16, 64><<<mblocks, 256, 0, s>>>(a, p.chunk, p.num_splits);
-  return cudaGetLastError();
+  if (a.d == 128) return launch_merge(decode_merge_kernel<__nv_bfloat16, 128>, a, p, s);
+  return launch_merge(decode_merge_kernel<__nv_bfloat16, 64>, a, p, s);
 }
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s) {
@@ -540,12 +617,8 @@ cudaError_t launch_decode_f32(const DecodeArgs& a, const DecodePlan& p, cudaStre
     decode_f32_kernel<64><<<grid, 128, 0, s>>>(a, p.chunk, p.num_splits);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.num_splits <= 1) return e;
-  const int mblocks = (a.B * a.Hq + 7) / 8;
-  if (a.d == 128)
-    decode_merge_kernel<float, 128><<<mblocks, 256, 0, s>>>(a, p.chunk, p.num_splits);
-  else
-    decode_merge_kernel<float, 64><<<mblocks, 256, 0, s>>>(a, p.chunk, p.num_splits);
-  return cudaGetLastError();
+  if (a.d == 128) return launch_merge(decode_merge_kernel<float, 128>, a, p, s);
+  return launch_merge(decode_merge_kernel<float, 64>, a, p, s);
 }
 
 }  // namespace pa

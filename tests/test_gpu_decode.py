@@ -49,6 +49,30 @@ def test_decode_bf16(lengths, hq, hkv, d, num_splits):
     assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
 
 
+def _short_lengths(n, hi, seed):
+    g = np.random.default_rng(seed)
+    base = [0, 1, 15, 16, 17, 33, hi]  # empty, one token, page edges, the longest
+    return base + [int(x) for x in g.integers(1, hi + 1, n - len(base))]
+
+
+@pytest.mark.parametrize("b,hq,hkv,d,hi,window", [
+    (40, 4, 4, 64, 1000, 0),     # MHA: 160 (sequence, KV head) pairs
+    (20, 64, 8, 128, 2048, 0),   # GQA 8, contexts up to the 128-block limit
+    (40, 8, 4, 128, 700, 100),   # window
+    (80, 64, 2, 64, 300, 0),     # G = 32: two 16-row tiles per KV head
+])
+def test_decode_bf16_short_context_warp_split(b, hq, hkv, d, hi, window):
+    """Short contexts with at least one (sequence, KV head) pair per SM take
+    the plan that deals a head's blocks to several warps of one CTA and merges
+    their states on chip (no range split, no merge kernel). Ragged lengths
+    include empty sequences and sequences with fewer blocks than warps."""
+    lengths = _short_lengths(b, hi, b + hq + d)
+    o, lse, want_o, want_lse = run_case(lengths, hq, hkv, d, torch.bfloat16, window=window,
+                                        seed=b + hkv)
+    assert_close_bf16(o, want_o, "o")
+    assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
+
+
 @pytest.mark.parametrize("window", [1, 16, 17, 100])
 @pytest.mark.parametrize("num_splits", [0, 2])
 def test_decode_bf16_window(window, num_splits):
