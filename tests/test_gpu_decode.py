@@ -61,11 +61,10 @@ def _short_lengths(n, hi, seed):
     (40, 8, 4, 128, 700, 100),   # window
     (80, 64, 2, 64, 300, 0),     # G = 32: two 16-row tiles per KV head
 ])
-def test_decode_bf16_short_context_warp_split(b, hq, hkv, d, hi, window):
-    """Short contexts with at least one (sequence, KV head) pair per SM take
-    the plan that deals a head's blocks to several warps of one CTA and merges
-    their states on chip (no range split, no merge kernel). Ragged lengths
-    include empty sequences and sequences with fewer blocks than warps."""
+def test_decode_bf16_many_short_sequences(b, hq, hkv, d, hi, window):
+    """Many short contexts (at least one (sequence, KV head) pair per SM):
+    ragged lengths including empty sequences and sequences shorter than one
+    range, a window, and two 16-row tiles per KV head."""
     lengths = _short_lengths(b, hi, b + hq + d)
     o, lse, want_o, want_lse = run_case(lengths, hq, hkv, d, torch.bfloat16, window=window,
                                         seed=b + hkv)
