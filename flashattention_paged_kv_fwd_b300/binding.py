@@ -31,7 +31,7 @@ PA_BF16 = 0
 PA_F32 = 1
 _DTYPES = {torch.bfloat16: PA_BF16, torch.float32: PA_F32}
 DEV_ERRORS = {1: "block id outside the pool", 2: "position beyond the block table",
-              4: "bounded wait gave up"}
+              4: "bounded wait gave up", 8: "unusable launch state (misaligned shared memory)"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -61,6 +61,9 @@ def load_library():
     lib.pa_attn_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, i32, i32,
                                     i32, f32, i32, vp, vp]
     lib.pa_attn_prefill.restype = i32
+    lib.pa_attn_prefill_paged.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, i32,
+                                          i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp]
+    lib.pa_attn_prefill_paged.restype = i32
     lib.pa_kv_append_paged.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                        i32, i32, vp, vp]
     lib.pa_kv_append_paged.restype = i32
@@ -199,6 +202,51 @@ def decode_workspace_bytes(batch, num_heads, num_kv_heads, head_dim, max_blocks_
     return int(load_library().pa_decode_workspace_bytes(batch, num_heads, num_kv_heads, head_dim,
                                                         max_blocks_per_seq, block_size,
                                                         int(window or 0), num_splits))
+
+
+def attn_prefill_paged(q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q, max_seqlen_q,
+                       *, causal=True, window=0, scale=None, out=None, lse=None,
+                       return_lse=True, err_flag=None, stream=None):
+    """Chunked prefill / prefix reuse: each sequence's packed queries over its
+    whole paged cache (the chunk's own keys appended first).
+
+    q [total_q, Hq, d] bf16; pools [num_blocks, 16, Hkv, d]; block_table int32
+    [B, max_blocks]; seq_lens int32 [B] = keys cached per sequence, the
+    chunk included; cu_seqlens_q int32 [B+1]. Query row i of a sequence with
+    Lq queries sits at position seq_lens[b] - Lq + i. Returns (o, lse [Hq,
+    total_q]).
+    """
+    lib = load_library()
+    _need(q.dtype == torch.bfloat16, "paged prefill takes bfloat16")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda_contig(name, t, q.dtype)
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens),
+                    ("cu_seqlens_q", cu_seqlens_q)):
+        _cuda_contig(name, t, torch.int32)
+    total_q, hq, d = q.shape
+    num_blocks, block_size, hkv, dk = k_cache.shape
+    _need(dk == d and v_cache.shape == k_cache.shape, "pool shapes do not match q")
+    B = cu_seqlens_q.numel() - 1
+    _need(block_table.dim() == 2 and block_table.shape[0] == B, "block_table must be [B, max_blocks]")
+    _need(seq_lens.numel() == B, "seq_lens must have B entries")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda_contig("out", out, q.dtype)
+        _need(out.shape == q.shape, "out must match q")
+    if lse is None and return_lse:
+        lse = torch.empty((hq, total_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _cuda_contig("lse", lse, torch.float32)
+        _need(lse.shape == (hq, total_q), "lse must be [Hq, total_q]")
+    st = lib.pa_attn_prefill_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                   block_table.shape[1], _ptr(seq_lens), _ptr(cu_seqlens_q),
+                                   total_q, int(max_seqlen_q), _ptr(out), _ptr(lse), B, hq, hkv,
+                                   d, block_size, num_blocks, 1 if causal else 0,
+                                   int(window or 0), float(scale or 0.0), _DTYPES[q.dtype],
+                                   _ptr(err_flag), _stream(stream))
+    _check(st, "attn_prefill_paged")
+    return out, lse
 
 
 def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, *, window=0, scale=None,

@@ -152,6 +152,47 @@ int pa_attn_prefill(const void* q, const void* k, const void* v, void* o, float*
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+int pa_attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, const int32_t* cu_seqlens_q, int total_q,
+                          int max_seqlen_q, void* o, float* lse, int B, int Hq, int Hkv, int d,
+                          int block_size, int num_blocks, int causal, int window, float scale,
+                          pa_dtype dtype, int32_t* err_flag, void* stream) {
+  if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || total_q < 0 || max_seqlen_q < 0 ||
+      num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_BF16 || block_size != 16) return PA_ERR_UNSUPPORTED;
+  if (window > 0 && !causal) return PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
+    return PA_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !cu_seqlens_q || !o)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(cu_seqlens_q, 4) ||
+      (lse && !aligned(lse, 4)) || (err_flag && !aligned(err_flag, 4)))
+    return PA_ERR_INVALID_ARG;
+  if (total_q == 0 || max_seqlen_q == 0) return PA_OK;
+
+  pa::PrefillArgs a{};
+  a.q = q; a.k = k_cache; a.v = v_cache; a.o = o; a.lse = lse; a.cu_seqlens = cu_seqlens_q;
+  a.err = err_flag;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.N = total_q; a.T = total_q; a.d = d;
+  a.max_seqlen = max_seqlen_q; a.causal = causal ? 1 : 0; a.window = window > 0 ? window : 0;
+  a.scale_log2 = scale_log2(scale, d);
+  a.table = block_table; a.seq_lens_k = seq_lens;
+  a.max_blocks = max_blocks_per_seq; a.num_blocks = num_blocks;
+  CUtensorMap qm, km, vm;
+  if (!encode_3d(&qm, q, d, Hq, total_q, 128) ||
+      !encode_pool(&km, k_cache, d, Hkv, block_size, num_blocks, 1) ||
+      !encode_pool(&vm, v_cache, d, Hkv, block_size, num_blocks, 1))
+    return PA_ERR_CUDA;
+  const cudaError_t e =
+      pa::launch_prefill_bf16(a, qm, km, vm, sm_count(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int pa_kv_append_paged(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                        const int32_t* block_table, int max_blocks_per_seq,
                        const int32_t* seq_lens, const int32_t* cu_new, int num_new_tokens,

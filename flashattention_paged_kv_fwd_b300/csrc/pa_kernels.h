@@ -68,11 +68,20 @@ struct PrefillArgs {
   int pair_heads;  // bf16 path: a work unit pairs two query heads (else two row tiles)
   int n_units;     // bf16 path: work units in the launch
   int compact;     // bf16 path: build the sorted on-chip work list (packed sequences)
+  // paged keys (prefill into a non-empty cache): keys and values of sequence b
+  // are its first seq_lens_k[b] tokens in the pools [num_blocks, 16, Hkv, d]
+  // addressed through table[b][*]; query row i of its Lq rows sits at
+  // position seq_lens_k[b] - Lq + i. k / v above are then the pools.
+  const int32_t* table;       // nullptr => contiguous keys (rows of k / v)
+  const int32_t* seq_lens_k;
+  int max_blocks, num_blocks;
 };
 
 // Work units of the bf16 prefill (two 128-row query tiles each).
 long long prefill_units(int B, int Hq, int Hkv, int max_seqlen, bool* pair_heads);
 
+// kmap / vmap: 3-D maps over [T, Hkv, d] rows, or -- with a.table -- 4-D maps
+// over the pools ordered (d, token, head, block) with 64 x 16 x 1 x 1 boxes.
 cudaError_t launch_prefill_bf16(const PrefillArgs& a, const CUtensorMap& qmap,
                                 const CUtensorMap& kmap, const CUtensorMap& vmap, int num_sms,
                                 cudaStream_t s);

@@ -106,7 +106,10 @@ static_assert(PfCfg<64>::SMEM <= 227 * 1024, "prefill d=64 shared memory");
 
 // One work unit: two query tiles sharing a KV head and a key range.
 struct Unit {
-  int start, len;  // packed row offset and length of the sequence
+  int start, len;  // packed row offset and number of query rows of the sequence
+  int lk;          // keys of the sequence (= len unless the keys are paged)
+  int qoff;        // position of query row 0 among the keys (lk - len when paged)
+  int b;           // sequence
   int q0[2];       // first row (within the sequence) of each query tile
   int h[2];        // query head of each tile
   int kvh;
@@ -137,12 +140,22 @@ __device__ __forceinline__ bool decode_unit(const PrefillArgs& a, int level, int
     w.start = b * a.N;
     w.len = a.N;
   }
+  w.b = b;
+  w.lk = w.len;
+  w.qoff = 0;
+  if (a.table) {
+    // keys from the paged cache: the last len of them are this chunk's own
+    w.lk = min(max(a.seq_lens_k[b], 0), a.max_blocks * 16);
+    w.qoff = w.lk - w.len;  // < 0 only on bad input (raised by the caller check)
+  }
   w.q0[0] = qt0 * BM;
   w.q0[1] = qt1 * BM;
   if (w.q0[0] >= w.len) return false;
   const int q_last = min(w.len, w.q0[1] + BM) - 1;  // last row of either tile
-  const int kv_end = a.causal ? q_last + 1 : w.len;
-  const int kv_begin = a.window > 0 ? max(0, w.q0[0] - a.window + 1) : 0;
+  int kv_end = a.causal ? min(w.lk, w.qoff + q_last + 1) : w.lk;
+  int kv_begin = a.window > 0 ? max(0, w.qoff + w.q0[0] - a.window + 1) : 0;
+  kv_end = max(kv_end, 1);  // at least one (possibly fully masked) key tile
+  kv_begin = min(kv_begin, kv_end - 1);
   w.t_begin = kv_begin / BN;
   w.n_tiles = (kv_end + BN - 1) / BN - w.t_begin;
   w.kvh = w.h[0] / (a.Hq / a.Hkv);
@@ -233,7 +246,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
 
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for copies / MMAs already in flight
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap kmap,
@@ -353,6 +366,40 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       return true;
     };
+    // Paged keys: a tile of 128 keys is 8 blocks of 16; lane t < 8 copies
+    // block t (one 16-row box per 64-column panel) straight to its rows of
+    // the slot. Blocks past the sequence's keys are not loaded.
+    auto load_tile_paged = [&](const CUtensorMap* m, int key0, const Unit& w) -> bool {
+      if (issued >= C::NSLOT && !warp_wait(bar(C::B_EMPTY + slot), phase ^ 1u, abort_flag))
+        return false;
+      const int pg = key0 / 16 + lane;
+      bool have = lane < BN / 16 && pg * 16 < w.lk;
+      int blk = -1;
+      if (have) {
+        blk = a.table[static_cast<int64_t>(w.b) * a.max_blocks + pg];
+        if (blk < 0 || blk >= a.num_blocks) {
+          raise_err(a.err, kDevErrBadBlock);
+          have = false;
+        }
+      }
+      const unsigned n = __popc(__ballot_sync(0xFFFFFFFFu, have));
+      const uint32_t fb = bar(C::B_FULL + slot);
+      if (leader) mbar_arrive_expect_tx(fb, n * (D / 64) * 16 * 128);
+      __syncwarp();
+      if (have) {
+#pragma unroll
+        for (int p = 0; p < D / 64; ++p)
+          tma_load_4d(sRing + slot * C::TB + p * C::PANEL_T + lane * 16 * 128, m, fb, p * 64, 0,
+                      w.kvh, blk);
+      }
+      __syncwarp();
+      ++issued;
+      if (++slot == C::NSLOT) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      return true;
+    };
     for (int k = 0; ok && k * G < n_units; ++k) {
       const int u = unit_of(k, cta, G);
       Unit w;
@@ -361,8 +408,11 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       sched.map(u, lv, sb, pr);
       if (!decode_unit(a, lv, sb, pr, w)) continue;
       for (int j = 0; ok && j < w.n_tiles; ++j) {
-        const int row = w.start + (w.t_begin + j) * BN;
-        ok = load_tile(&kmap, row, w.kvh) && load_tile(&vmap, row, w.kvh);
+        const int key0 = (w.t_begin + j) * BN;
+        if constexpr (PAGED)
+          ok = load_tile_paged(&kmap, key0, w) && load_tile_paged(&vmap, key0, w);
+        else
+          ok = load_tile(&kmap, w.start + key0, w.kvh) && load_tile(&vmap, w.start + key0, w.kvh);
         if (ok && j == 0) {
           // the first K/V tiles go out before the Q tiles, which wait for the
           // previous unit's last QK^T
@@ -474,7 +524,23 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       release();  // K(0)
       if (n == 1) commit(C::B_QFREE + 1);
       for (int j = 0; j < n; ++j, ++tc) {
-        if (!(ok = wait_full(vs) && pv(0, vs, j > 0 ? 1u : 0u))) break;
+        if (!(ok = wait_full(vs))) break;
+        if constexpr (PAGED) {
+          // slots past the sequence's keys may hold anything (even NaN): P is
+          // 0 there, but 0 * NaN is not, so those V rows are cleared first
+          const int valid = w.lk - (w.t_begin + j) * BN;
+          if (valid < BN) {
+            const int r0 = valid > 0 ? valid : 0;
+            uint8_t* vt = gb + C::OFF_RING + vs * C::TB;
+            for (int e = r0 * 8 + lane; e < BN * 8; e += 32)  // 16-byte pieces of 128-byte rows
+#pragma unroll
+              for (int p = 0; p < D / 64; ++p)
+                *reinterpret_cast<uint4*>(vt + p * C::PANEL_T + e * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (!(ok = pv(0, vs, j > 0 ? 1u : 0u))) break;
         if (j == n - 1) commit(C::B_OFULL + 0);
         if (j + 1 < n) {
           if (!(ok = wait_full(ks))) break;
@@ -518,7 +584,9 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       sched.map(u, lv, sb, pr);
       if (!decode_unit(a, lv, sb, pr, w)) continue;
       const int q0 = w.q0[ti];
-      const int i_abs = q0 + r;  // query position in its sequence
+      const int q_row = q0 + r;            // query row within its sequence
+      const int i_abs = w.qoff + q_row;    // its position among the keys
+      const int p0 = w.qoff + q0;          // position of the tile's first row
       float m = kNegInf, l = 0.f;
       for (int j = 0; j < w.n_tiles; ++j, ++tc) {
         if (!(ok = warp_wait(bar(C::B_SFULL + ti), tc & 1, abort_flag))) break;
@@ -530,13 +598,13 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         tmem_wait_ld();
 
         const int kt0 = (w.t_begin + j) * BN;
-        const bool need_mask = (kt0 + BN > w.len) || (a.causal && kt0 + BN - 1 > q0) ||
-                               (a.window > 0 && kt0 <= q0 + BM - 1 - a.window);
+        const bool need_mask = (kt0 + BN > w.lk) || (a.causal && kt0 + BN - 1 > p0) ||
+                               (a.window > 0 && kt0 <= p0 + BM - 1 - a.window);
         if (need_mask) {
 #pragma unroll
           for (int c = 0; c < BN; ++c) {
             const int jk = kt0 + c;
-            const bool vis = jk < w.len && (!a.causal || jk <= i_abs) &&
+            const bool vis = jk < w.lk && (!a.causal || jk <= i_abs) &&
                              (a.window <= 0 || jk > i_abs - a.window);
             if (!vis) sr[c] = __float_as_uint(kNegInf);
           }
@@ -618,9 +686,9 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int h = w.h[ti];
-      const bool live = i_abs < w.len;
+      const bool live = q_row < w.len;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
-                            (static_cast<int64_t>(w.start + i_abs) * a.Hq + h) * D;
+                            (static_cast<int64_t>(w.start + q_row) * a.Hq + h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -641,7 +709,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         }
       }
       if (a.lse && live)
-        a.lse[static_cast<int64_t>(h) * a.T + w.start + i_abs] =
+        a.lse[static_cast<int64_t>(h) * a.T + w.start + q_row] =
             l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
       ++uc;
     }
@@ -716,18 +784,26 @@ __global__ void __launch_bounds__(128) prefill_f32_kernel(const PrefillArgs a) {
     a.lse[static_cast<int64_t>(h) * a.T + tok] = l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
 }
 
-int g_pf_attr[2][64];
+int g_pf_attr[4][64];
 
-template <int D>
+template <int D, bool PAGED>
 void ensure_pf_attr() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (!g_pf_attr[D == 128][dev]) {
-    cudaFuncSetAttribute(prefill_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         PfCfg<D>::SMEM);
-    g_pf_attr[D == 128][dev] = 1;
+  const int v = (D == 128) + 2 * PAGED;
+  if (!g_pf_attr[v][dev]) {
+    cudaFuncSetAttribute(prefill_bf16_kernel<D, PAGED>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<D>::SMEM);
+    g_pf_attr[v][dev] = 1;
   }
+}
+
+template <int D, bool PAGED>
+void launch_pf(unsigned grid, const CUtensorMap& qmap, const CUtensorMap& kmap,
+               const CUtensorMap& vmap, const PrefillArgs& a, cudaStream_t s) {
+  ensure_pf_attr<D, PAGED>();
+  prefill_bf16_kernel<D, PAGED><<<grid, kThreads, PfCfg<D>::SMEM, s>>>(qmap, kmap, vmap, a);
 }
 
 }  // namespace
@@ -753,12 +829,13 @@ cudaError_t launch_prefill_bf16(const PrefillArgs& a0, const CUtensorMap& qmap,
   a.n_units = static_cast<int>(units);
   a.compact = (a.cu_seqlens && a.B <= kMaxSchedSeqs && (a.max_seqlen + BM - 1) / BM <= 65535) ? 1 : 0;
   const unsigned grid = static_cast<unsigned>(units < num_sms ? units : num_sms);
+  const bool paged = a.table != nullptr;
   if (a.d == 128) {
-    ensure_pf_attr<128>();
-    prefill_bf16_kernel<128><<<grid, kThreads, PfCfg<128>::SMEM, s>>>(qmap, kmap, vmap, a);
+    if (paged) launch_pf<128, true>(grid, qmap, kmap, vmap, a, s);
+    else launch_pf<128, false>(grid, qmap, kmap, vmap, a, s);
   } else {
-    ensure_pf_attr<64>();
-    prefill_bf16_kernel<64><<<grid, kThreads, PfCfg<64>::SMEM, s>>>(qmap, kmap, vmap, a);
+    if (paged) launch_pf<64, true>(grid, qmap, kmap, vmap, a, s);
+    else launch_pf<64, false>(grid, qmap, kmap, vmap, a, s);
   }
   return cudaGetLastError();
 }

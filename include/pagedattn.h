@@ -112,6 +112,44 @@ PA_API int pa_attn_prefill(const void* q, const void* k, const void* v, void* o,
                     void* stream);
 
 /*
+ * attn_prefill_paged -- a chunk of new queries per sequence attending to the
+ * sequence's whole paged cache: chunked prefill, or a prompt whose prefix is
+ * already cached. "Генерация и KV-кэш", section "Три ловушки, на которых
+ * спотыкаются все", trap 2 (queries that continue a cache are aligned to the
+ * bottom-right corner of the score matrix); "Module 09: Efficient Attention",
+ * sections "Code: A Paged KV Cache from Scratch" and "The Block Table" (key
+ * t of a sequence is (block_table[t / 16], t % 16) of the pools).
+ * Sequence b holds seq_lens[b] keys in the cache; its Lq_b =
+ * cu_seqlens_q[b+1] - cu_seqlens_q[b] queries are the LAST Lq_b of those
+ * positions (append the chunk's keys and values with pa_kv_append_paged
+ * first), so query row i sits at position p_i = seq_lens[b] - Lq_b + i and
+ * the visibility rules of attn_prefill apply with that p_i.
+ *
+ *  q     [total_q, Hq, d]   packed queries (bf16), token-major
+ *  k_cache, v_cache [num_blocks, 16, Hkv, d] pools (bf16), read only
+ *  block_table int32 [B, max_blocks_per_seq]; entries past a sequence's
+ *        last block are never read (any value)
+ *  seq_lens   int32 [B]: keys of each sequence, the chunk's own included
+ *        (>= its Lq; <= max_blocks_per_seq * 16)
+ *  cu_seqlens_q int32 [B+1]: packed offsets of the queries; total_q =
+ *        cu_seqlens_q[B]; max_seqlen_q bounds every Lq_b
+ *  o     [total_q, Hq, d] output (bf16); lse [Hq, total_q] float32 or NULL
+ *  block_size must be 16; dtype must be PA_BF16 (PA_ERR_UNSUPPORTED
+ *  otherwise). causal / window / scale as in attn_prefill.
+ * Slots of a block past a sequence's keys may hold anything (even NaN): they
+ * are never used. A block id outside [0, num_blocks) raises PA_DEV_BAD_BLOCK
+ * and that block is skipped. Alignment: q, pools, o 16-byte aligned; int32
+ * arrays and lse 4-byte aligned.
+ */
+PA_API int pa_attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_table, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                                 int total_q, int max_seqlen_q, void* o, float* lse, int B,
+                                 int Hq, int Hkv, int d, int block_size, int num_blocks,
+                                 int causal, int window, float scale, pa_dtype dtype,
+                                 int32_t* err_flag, void* stream);
+
+/*
  * kv_append_paged -- write new tokens' keys and values into the paged pools.
  * "Module 09: Efficient Attention", section "Code: A Paged KV Cache from
  * Scratch": token t of a sequence lives at (block_table[t / block_size],

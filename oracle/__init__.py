@@ -35,6 +35,7 @@ from .paged import (
     gather_paged,
     append_paged,
     decode_paged,
+    prefill_paged,
 )
 from .kv_bytes import kv_cache_bytes, kv_bytes_per_token_per_layer
 
@@ -49,6 +50,7 @@ __all__ = [
     "gather_paged",
     "append_paged",
     "decode_paged",
+    "prefill_paged",
     "kv_cache_bytes",
     "kv_bytes_per_token_per_layer",
 ]

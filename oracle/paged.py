@@ -18,13 +18,19 @@ Decode semantics ("–ì–µ–Ω–µ—Ä–∞—Ü–∏—è –∏ KV-–∫—ç—à", sections "–î–≤–µ —Ñ–∞–∑—ã –
 –∏ decode" and "KV-–∫—ç—à –¥–ª—è –æ–¥–Ω–æ–π –≥–æ–ª–æ–≤—ã –Ω–∞ NumPy"): the new token's k, v are
 written to the cache first, then its single query attends over every cached
 key (itself included), so no mask is needed beyond the sliding window.
+
+Chunked prefill / prefix reuse (same lesson, section "–¢—Ä–∏ –ª–æ–≤—É—à–∫–∏, –Ω–∞ –∫–æ—Ç–æ—Ä—ã—Ö
+—Å–ø–æ—Ç—ã–∫–∞—é—Ç—Å—è –≤—Å–µ", trap 2: a query block that continues a cache is aligned to
+the bottom-right of the score matrix): a chunk's Lq queries are the last Lq of
+the sequence's Lk cached positions, so query i sits at position Lk - Lq + i
+and sees the keys the causal (and window) rule allows from there.
 """
 
 import numpy as np
 
 from .attention import _as_f64, sdpa
 
-__all__ = ["paged_slot", "gather_paged", "append_paged", "decode_paged"]
+__all__ = ["paged_slot", "gather_paged", "append_paged", "decode_paged", "prefill_paged"]
 
 
 def paged_slot(block_table_row, position, block_size):
@@ -100,4 +106,37 @@ def decode_paged(q, k_pool, v_pool, block_table, seq_lens, *, block_size, window
         ob, lb = sdpa(q[b:b + 1], k, v, causal=True, window=window, scale=scale)
         o[b] = ob[0]
         lse[:, b] = lb[:, 0]
+    return o, lse
+
+
+def prefill_paged(q, k_pool, v_pool, block_table, seq_lens, cu_seqlens_q, *, block_size,
+                  causal=True, window=0, scale=None, batch_indices=None):
+    """Each sequence's chunk of queries over its whole paged cache.
+
+    q: [total_q, Hq, d] packed; sequence b's queries are rows
+    cu_seqlens_q[b] .. cu_seqlens_q[b+1] and sit at the last positions of its
+    seq_lens[b] cached keys (bottom-right alignment). Keys and values are
+    gathered token by token through the block table, then the plain softmax
+    of ``sdpa`` runs on the full score matrix. Returns o [total_q, Hq, d] and
+    lse [Hq, total_q] (float64); rows of sequences outside ``batch_indices``
+    stay zero / -inf.
+    """
+    q = _as_f64(q)
+    total, hq, d = q.shape
+    o = np.zeros((total, hq, d), dtype=np.float64)
+    lse = np.full((hq, total), -np.inf, dtype=np.float64)
+    n_seq = len(seq_lens)
+    todo = range(n_seq) if batch_indices is None else batch_indices
+    for b in todo:
+        q0, q1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
+        length = int(seq_lens[b])
+        if q1 == q0:
+            continue
+        if length < q1 - q0:
+            raise ValueError("a chunk cannot hold more queries than the cache holds keys")
+        k = _as_f64(gather_paged(k_pool, block_table[b], length, block_size))
+        v = _as_f64(gather_paged(v_pool, block_table[b], length, block_size))
+        ob, lb = sdpa(q[q0:q1], k, v, causal=causal, window=window, scale=scale)
+        o[q0:q1] = ob
+        lse[:, q0:q1] = lb
     return o, lse

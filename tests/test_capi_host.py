@@ -32,8 +32,8 @@ def declared_symbols():
 
 def test_header_declares_the_entry_points():
     syms = declared_symbols()
-    for name in ("pa_attn_prefill", "pa_kv_append_paged", "pa_attn_decode_paged",
-                 "pa_decode_workspace_bytes", "pa_status_str"):
+    for name in ("pa_attn_prefill", "pa_attn_prefill_paged", "pa_kv_append_paged",
+                 "pa_attn_decode_paged", "pa_decode_workspace_bytes", "pa_status_str"):
         assert name in syms
 
 
@@ -73,6 +73,29 @@ def test_prefill_host_validation(lib):
     assert _prefill(lib, dt=7) == PA_ERR_INVALID_ARG
     assert _prefill(lib, causal=0, window=8) == PA_ERR_UNSUPPORTED
     assert _prefill(lib, N=0) == PA_OK                            # nothing to do, no launch
+
+
+def _prefill_paged(lib, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, table=FAKE, mb=8, sl=FAKE, cu=FAKE, tq=16, msl=16, o=FAKE,
+             lse=None, B=2, Hq=4, Hkv=2, d=64, bs=16, nb=16, causal=1, window=0, scale=0.0,
+             dt=0, err=None, stream=None)
+    a.update(kw)
+    return lib.pa_attn_prefill_paged(a["q"], a["kc"], a["vc"], a["table"], a["mb"], a["sl"],
+                                     a["cu"], a["tq"], a["msl"], a["o"], a["lse"], a["B"],
+                                     a["Hq"], a["Hkv"], a["d"], a["bs"], a["nb"], a["causal"],
+                                     a["window"], a["scale"], a["dt"], a["err"], a["stream"])
+
+
+def test_prefill_paged_host_validation(lib):
+    assert _prefill_paged(lib, Hq=6, Hkv=4) == PA_ERR_INVALID_ARG
+    assert _prefill_paged(lib, d=32) == PA_ERR_INVALID_ARG
+    assert _prefill_paged(lib, cu=None) == PA_ERR_INVALID_ARG       # packed queries required
+    assert _prefill_paged(lib, table=None) == PA_ERR_INVALID_ARG
+    assert _prefill_paged(lib, kc=FAKE + 8) == PA_ERR_INVALID_ARG   # 16-byte alignment
+    assert _prefill_paged(lib, bs=32) == PA_ERR_UNSUPPORTED          # pages of 16 tokens
+    assert _prefill_paged(lib, dt=1) == PA_ERR_UNSUPPORTED           # bf16 only
+    assert _prefill_paged(lib, causal=0, window=8) == PA_ERR_UNSUPPORTED
+    assert _prefill_paged(lib, tq=0) == PA_OK                       # nothing to do, no launch
 
 
 def _append(lib, **kw):

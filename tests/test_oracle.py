@@ -288,6 +288,57 @@ def test_window_decode_equals_full_forward():
         assert np.abs(lse[:, 0] - lse_full[:, t]).max() <= TOL
 
 
+def pin_chunked_prefill_equals_full():
+    """A sequence cached in a scattered pool and processed as three chunks
+    (each chunk's queries over everything cached so far, bottom-right
+    aligned) reproduces the rows of one causal forward over the whole
+    sequence, with and without a window; a one-query chunk is a decode step."""
+    lk, hq, hkv, d, bs = 70, 4, 2, 8, 16
+    q = _rand((lk, hq, d), 90)
+    k = _rand((lk, hkv, d), 91)
+    v = _rand((lk, hkv, d), 92)
+    table = np.array([[9, 3, 7, 1, 5]])
+    kc = np.full((10, bs, hkv, d), np.nan)
+    vc = np.full((10, bs, hkv, d), np.nan)
+    kc, vc = oracle.append_paged(kc, vc, k, v, table, [0], [0, lk], bs)
+    worst = 0.0
+    for win in (0, 20):
+        o_full, lse_full = oracle.sdpa(q, k, v, causal=True, window=win)
+        for a, b in ((0, 25), (25, 26), (26, 70)):
+            o, lse = oracle.prefill_paged(q[a:b], kc, vc, table, [b], [0, b - a], block_size=bs,
+                                          window=win)
+            worst = max(worst, float(np.abs(o - o_full[a:b]).max()),
+                        float(np.abs(lse - lse_full[:, a:b]).max()))
+        od, ld = oracle.decode_paged(q[40:41], kc, vc, table, [41], block_size=bs, window=win)
+        op, lp = oracle.prefill_paged(q[40:41], kc, vc, table, [41], [0, 1], block_size=bs,
+                                      window=win)
+        worst = max(worst, float(np.abs(od - op).max()), float(np.abs(ld - lp).max()))
+    return worst
+
+
+def test_chunked_prefill_equals_full_forward():
+    assert pin_chunked_prefill_equals_full() <= TOL
+
+
+def test_chunked_prefill_packed_sequences():
+    """Several sequences in one pool, packed queries: each sequence's rows
+    equal its own single-sequence result (gathered keys, bottom-right)."""
+    hq, hkv, d, bs = 4, 1, 8, 16
+    lks, lqs = [5, 40, 33], [5, 1, 17]
+    cu = np.cumsum([0] + lqs)
+    w = inputs.make_paged_cache(lks, lks, hkv, d, torch.float64, 93, "cpu", spare_blocks=1)
+    q = _rand((cu[-1], hq, d), 94)
+    table = w["block_table"].tolist()
+    o, lse = oracle.prefill_paged(q, w["k_cache"], w["v_cache"], table, lks, cu, block_size=bs,
+                                  causal=True)
+    for b in range(3):
+        k = oracle.gather_paged(w["k_cache"], table[b], lks[b], bs).numpy()
+        v = oracle.gather_paged(w["v_cache"], table[b], lks[b], bs).numpy()
+        ob, lb = oracle.sdpa(q[cu[b]:cu[b + 1]], k, v, causal=True)
+        assert np.abs(o[cu[b]:cu[b + 1]] - ob).max() <= TOL
+        assert np.abs(lse[:, cu[b]:cu[b + 1]] - lb).max() <= TOL
+
+
 def test_sdpa_rows_and_varlen_agree_with_sdpa():
     lens = [5, 1, 12]
     cu = np.cumsum([0] + lens)
@@ -423,6 +474,7 @@ def _all_pins(golden):
         "gqa": pin_gqa_is_repeat_interleave(),
         "align": pin_bottom_right_alignment(),
         "cache": pin_cached_decode_equals_full(),
+        "chunked": pin_chunked_prefill_equals_full(),
     }
 
 
