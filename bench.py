@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixed_window4096",
                     choices=["mixed_window4096", "gqa_decode_llama3_70b", "mha_decode_gpt2",
-                             "gqa_prefill_llama3_8b"],
+                             "gqa_prefill_llama3_8b", "chunked_prefill_llama3_8b"],
                     help="other workloads time a single kernel family (profiling aid)")
     ap.add_argument("--only", choices=["prefill", "append", "decode"], default=None,
                     help="run only one phase of the mixed step (profiling aid)")
@@ -188,6 +188,13 @@ def prefill_flops(lengths, hq, d, window):
     return 4.0 * d * hq * pairs
 
 
+def chunked_prefill_flops(prefixes, chunk, hq, d):
+    """4*d FLOPs per visible (query, key) pair and query head: query i of a
+    chunk after a cached prefix p sees p + i + 1 keys (causal)."""
+    pairs = sum(chunk * p + chunk * (chunk + 1) // 2 for p in prefixes)
+    return 4.0 * d * hq * pairs
+
+
 def decode_bytes(lengths, hkv, d, window, elem=2):
     """Keys and values of every visible token, read once (2 * Hkv * d * elem per
     token and sequence)."""
@@ -267,7 +274,16 @@ class SingleStep:
         self.b = binding
         self.name = name
         self.err = binding.new_err_flag(device)
-        if name == "gqa_prefill_llama3_8b":
+        if name == "chunked_prefill_llama3_8b":
+            w = inputs.chunked_prefill_llama3_8b(device)
+            self.w = w
+            self.out = torch.empty_like(w["q"])
+            self.lse = torch.empty((w["hq"], w["q"].shape[0]), dtype=torch.float32, device=device)
+            self.flops = chunked_prefill_flops(w["prefixes"], w["chunk"], w["hq"], w["d"])
+            self.dbytes = 0.0
+            self.phase = "prefill"
+            self.launches = {"prefill": 1}
+        elif name == "gqa_prefill_llama3_8b":
             w = inputs.gqa_prefill_llama3_8b(device)
             self.w = w
             self.out = torch.empty_like(w["q"])
@@ -294,7 +310,11 @@ class SingleStep:
 
     def run(self):
         w = self.w
-        if self.phase == "prefill":
+        if self.name == "chunked_prefill_llama3_8b":
+            self.b.attn_prefill_paged(w["q"], w["k_cache"], w["v_cache"], w["block_table"],
+                                      w["seq_lens"], w["cu_seqlens_q"], w["chunk"],
+                                      out=self.out, lse=self.lse, err_flag=self.err)
+        elif self.phase == "prefill":
             self.b.attn_prefill(w["q"], w["k"], w["v"], causal=True, cu_seqlens=w["cu_seqlens"],
                                 max_seqlen=w["max_seqlen"], out=self.out, lse=self.lse,
                                 err_flag=self.err)
@@ -555,6 +575,11 @@ def run_ours(args):
                     "l2": L2_NOTE})
         if args.only:
             cfg["only"] = args.only
+    elif args.workload == "chunked_prefill_llama3_8b":
+        w = st.w
+        cfg.update({"hq": 32, "hkv": 8, "d": 128, "block_size": 16, "sequences": len(w["prefixes"]),
+                    "chunk": w["chunk"], "cached_prefix_tokens": int(sum(w["prefixes"])),
+                    "l2": L2_NOTE})
     else:
         cfg.update({"l2": L2_NOTE})
     line = {

@@ -43,6 +43,7 @@ __all__ = [
     "gqa_prefill_llama3_8b",
     "gqa_decode_llama3_70b",
     "mixed_window4096",
+    "chunked_prefill_llama3_8b",
     "WORKLOADS",
 ]
 
@@ -55,6 +56,7 @@ WORKLOAD_SEEDS = {
     "gqa_prefill_llama3_8b": 1002,
     "gqa_decode_llama3_70b": 1003,
     "mixed_window4096": 1004,
+    "chunked_prefill_llama3_8b": 1005,
 }
 
 
@@ -233,10 +235,35 @@ def mixed_window4096(device="cpu", dtype=torch.bfloat16, poison=True, n_prefill=
     }
 
 
+def chunked_prefill_llama3_8b(device="cpu", dtype=torch.bfloat16, poison=True, batch=8,
+                              chunk=2048, prefix_lo=1024, prefix_hi=14336):
+    """Chunked prefill with cached prefixes, Llama-3-8B heads (Hq=32, Hkv=8,
+    d=128): each of `batch` sequences already caches a prefix of
+    U[prefix_lo, prefix_hi] tokens plus its new chunk of `chunk` tokens (the
+    chunk's keys and values appended), and the chunk's queries attend to all
+    of them, bottom-right aligned."""
+    seed = WORKLOAD_SEEDS["chunked_prefill_llama3_8b"]
+    hq, hkv, d = 32, 8, 128
+    prefixes = _uniform_ints(prefix_lo, prefix_hi, batch, make_generator(seed + 2))
+    lks = [p + chunk for p in prefixes]
+    cache = make_paged_cache(lks, lks, hkv, d, dtype, seed + 1, device, poison=poison)
+    gen = make_generator(seed + 3, device)
+    q = randn((batch * chunk, hq, d), dtype, gen, device)
+    cu = [i * chunk for i in range(batch + 1)]
+    return {
+        "hq": hq, "hkv": hkv, "d": d, "scale": 1.0 / math.sqrt(d), "q": q,
+        "prefixes": prefixes, "chunk": chunk, "lengths": lks,
+        "seq_lens": torch.tensor(lks, dtype=torch.int32, device=device),
+        "cu_seqlens_q": torch.tensor(cu, dtype=torch.int32, device=device),
+        **cache,
+    }
+
+
 WORKLOADS = {
     "gqa_tiny_f32": gqa_tiny_f32,
     "mha_decode_gpt2": mha_decode_gpt2,
     "gqa_prefill_llama3_8b": gqa_prefill_llama3_8b,
     "gqa_decode_llama3_70b": gqa_decode_llama3_70b,
     "mixed_window4096": mixed_window4096,
+    "chunked_prefill_llama3_8b": chunked_prefill_llama3_8b,
 }

@@ -106,3 +106,34 @@ def test_prefill_paged_reports_bad_block():
                                err_flag=err)
     with pytest.raises(binding.PagedAttnError, match="block id"):
         binding.check_err_flag(err)
+
+
+def test_prefill_paged_chunked_workload_full_size_sampled():
+    """The chunked-prefill launch the bench times (8 sequences, cached
+    prefixes U[1024, 14336] + chunks of 2048 queries, Llama-3-8B heads):
+    rows sampled at tile edges and at random, for heads of different KV
+    groups, against the oracle on the gathered keys."""
+    import numpy as np
+
+    w = inputs.chunked_prefill_llama3_8b("cuda")
+    err = binding.new_err_flag()
+    o, lse = binding.attn_prefill_paged(w["q"], w["k_cache"], w["v_cache"], w["block_table"],
+                                        w["seq_lens"], w["cu_seqlens_q"], w["chunk"],
+                                        err_flag=err)
+    binding.check_err_flag(err)
+    chunk = w["chunk"]
+    rng = np.random.default_rng(1)
+    picks = [0, 1, 127, 128, chunk - 1] + [int(x) for x in rng.integers(0, chunk, 4)]
+    heads = [0, 5, 31]
+    table = w["block_table"].cpu().tolist()
+    for b in (0, 5):
+        lk = w["lengths"][b]
+        k = oracle.gather_paged(w["k_cache"].cpu(), table[b], lk, 16)
+        v = oracle.gather_paged(w["v_cache"].cpu(), table[b], lk, 16)
+        qb = w["q"][b * chunk:(b + 1) * chunk].cpu()
+        rows = [(i, h) for i in picks for h in heads]
+        want_o, want_lse = oracle.sdpa_rows(qb, k, v, rows, causal=True)
+        got_o = torch.stack([o[b * chunk + i, h] for i, h in rows])
+        got_lse = torch.stack([lse[h, b * chunk + i] for i, h in rows])
+        assert_close_bf16(got_o, want_o, f"o[b={b}]")
+        assert_close(got_lse.cpu(), want_lse, f"lse[b={b}]", LSE_TOL)
