@@ -64,6 +64,8 @@ def load_library():
     lib.pa_attn_prefill_paged.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, vp, vp, i32,
                                           i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, vp]
     lib.pa_attn_prefill_paged.restype = i32
+    lib.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+    lib.pa_copy_blocks.restype = i32
     lib.pa_kv_append_paged.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                        i32, i32, vp, vp]
     lib.pa_kv_append_paged.restype = i32
@@ -247,6 +249,24 @@ def attn_prefill_paged(q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q,
                                    _ptr(err_flag), _stream(stream))
     _check(st, "attn_prefill_paged")
     return out, lse
+
+
+def copy_blocks(k_cache, v_cache, src_blocks, dst_blocks, *, err_flag=None, stream=None):
+    """Copy block src_blocks[i] over dst_blocks[i] in both pools (int32
+    device tensors of equal length), for copy-on-write of shared blocks."""
+    lib = load_library()
+    _need(k_cache.dtype in _DTYPES, "pools must be bfloat16 or float32")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda_contig(name, t, k_cache.dtype)
+    _need(v_cache.shape == k_cache.shape, "pool shapes differ")
+    for name, t in (("src_blocks", src_blocks), ("dst_blocks", dst_blocks)):
+        _cuda_contig(name, t, torch.int32)
+    _need(src_blocks.numel() == dst_blocks.numel(), "src and dst lists differ in length")
+    num_blocks, block_size, hkv, d = k_cache.shape
+    st = lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_blocks), _ptr(dst_blocks),
+                            src_blocks.numel(), block_size, hkv, d, num_blocks,
+                            _DTYPES[k_cache.dtype], _ptr(err_flag), _stream(stream))
+    _check(st, "copy_blocks")
 
 
 def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, *, window=0, scale=None,

@@ -218,6 +218,26 @@ int pa_kv_append_paged(const void* k_new, const void* v_new, void* k_cache, void
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_blocks,
+                   const int32_t* dst_blocks, int num_pairs, int block_size, int Hkv, int d,
+                   int num_blocks, pa_dtype dtype, int32_t* err_flag, void* stream) {
+  if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
+  if (num_pairs < 0 || block_size <= 0 || Hkv <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !src_blocks || !dst_blocks) return PA_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_blocks, 4) ||
+      !aligned(dst_blocks, 4) || (err_flag && !aligned(err_flag, 4)))
+    return PA_ERR_INVALID_ARG;
+  const long long block_bytes =
+      static_cast<long long>(block_size) * Hkv * d * static_cast<long long>(elem_size(dtype));
+  if (block_bytes % 16 != 0 || block_bytes / 16 > 0x7FFFFFFFLL) return PA_ERR_INVALID_ARG;
+  const cudaError_t e = pa::launch_copy_blocks(k_cache, v_cache, src_blocks, dst_blocks,
+                                               num_pairs, block_bytes, num_blocks, err_flag,
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int max_blocks_per_seq,
                                  int block_size, int window, int num_splits) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (d != 64 && d != 128) ||

@@ -14,6 +14,11 @@ cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache
                              const int32_t* cu_new, int n_tok, int n_seq, int row_bytes,
                              int block_size, int num_blocks, int32_t* err, cudaStream_t s);
 
+// ------------------------------------------------------------- block copy
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src,
+                               const int32_t* dst, int n_pairs, long long block_bytes,
+                               int num_blocks, int32_t* err, cudaStream_t s);
+
 // ------------------------------------------------------------------ decode
 // How one decode call is cut into CTAs. Each sequence's visible blocks
 // [first, last] are cut into ranges of `chunk` blocks; range s of sequence b

@@ -36,12 +36,14 @@ def contiguous_reserved_slots(max_seq_len, num_sequences):
 
 
 class BlockAllocator:
-    """Free list over ``num_blocks`` physical blocks.
+    """Free list over ``num_blocks`` physical blocks, with reference counts.
 
     ``allocate()`` pops the most recently freed (or highest-numbered initial)
-    block; ``free()`` returns one. ``num_free + num_used`` never changes.
-    An optional ``order`` gives the initial free list (for example a shuffled
-    permutation, so tables come out scattered).
+    block with one reference; ``share()`` adds a reference to an allocated
+    block; ``free()`` drops one and returns the block to the free list when
+    none is left. ``num_free + num_used`` never changes. An optional ``order``
+    gives the initial free list (for example a shuffled permutation, so tables
+    come out scattered).
     """
 
     def __init__(self, num_blocks, order=None):
@@ -52,7 +54,7 @@ class BlockAllocator:
             self._free = [int(b) for b in order]
             if sorted(self._free) != list(range(self.num_blocks)):
                 raise ValueError("order must be a permutation of range(num_blocks)")
-        self._used = set()
+        self._refs = {}
 
     @property
     def num_free(self):
@@ -60,20 +62,31 @@ class BlockAllocator:
 
     @property
     def num_used(self):
-        return len(self._used)
+        return len(self._refs)
+
+    def refcount(self, blk):
+        return self._refs.get(blk, 0)
 
     def allocate(self):
         if not self._free:
             raise MemoryError("no free KV blocks left")
         blk = self._free.pop()
-        self._used.add(blk)
+        self._refs[blk] = 1
+        return blk
+
+    def share(self, blk):
+        if blk not in self._refs:
+            raise ValueError(f"block {blk} is not allocated")
+        self._refs[blk] += 1
         return blk
 
     def free(self, blk):
-        if blk not in self._used:
+        if blk not in self._refs:
             raise ValueError(f"block {blk} is not allocated")
-        self._used.remove(blk)
-        self._free.append(blk)
+        self._refs[blk] -= 1
+        if self._refs[blk] == 0:
+            del self._refs[blk]
+            self._free.append(blk)
 
 
 class SequenceTables:
@@ -106,6 +119,40 @@ class SequenceTables:
             table.append(self.allocator.allocate())
         self.lengths[seq] = max(self.lengths[seq], new_len)
         return table
+
+    def share_prefix(self, src, num_prefix_blocks):
+        """A new sequence that points at the first ``num_prefix_blocks``
+        blocks of ``src`` (no block is copied or allocated); it holds
+        min(len(src), num_prefix_blocks * block_size) tokens."""
+        blocks = self.tables[src][:num_prefix_blocks]
+        if len(blocks) < num_prefix_blocks:
+            raise ValueError("the source sequence has fewer blocks")
+        seq = self.add_sequence()
+        self.tables[seq] = [self.allocator.share(b) for b in blocks]
+        self.lengths[seq] = min(self.lengths[src], num_prefix_blocks * self.block_size)
+        return seq
+
+    def prepare_write(self, seq, new_len):
+        """Make positions [len(seq), new_len) writable: every block those
+        positions fall in that another sequence still references is replaced
+        by a private copy, then blocks are claimed up to ``new_len``. Returns
+        the (source, destination) block pairs the device must copy first
+        (``pa_copy_blocks``), in table order."""
+        table = self.tables[seq]
+        start = self.lengths[seq]
+        copies = []
+        if new_len > start:
+            first = start // self.block_size
+            last = min(blocks_needed(new_len, self.block_size), len(table))
+            for i in range(first, last):
+                old = table[i]
+                if self.allocator.refcount(old) > 1:
+                    new = self.allocator.allocate()
+                    self.allocator.free(old)  # drops this sequence's reference
+                    table[i] = new
+                    copies.append((old, new))
+        self.reserve(seq, new_len)
+        return copies
 
     def release(self, seq):
         for blk in self.tables.pop(seq):

@@ -177,6 +177,29 @@ PA_API int pa_kv_append_paged(const void* k_new, const void* v_new, void* k_cach
                        int32_t* err_flag, void* stream);
 
 /*
+ * copy_blocks -- copy whole blocks of both pools (keys and values), for
+ * copy-on-write of shared prefix blocks. "Module 09: Efficient Attention",
+ * section "Sharing Blocks: Copy-on-Write": sequences sharing a prefix point
+ * at the same physical blocks, with a per-block reference count; before a
+ * sharer writes into a shared block, that one block is copied and the
+ * sharer's table is pointed at the copy. The reference counting and table
+ * updates are the caller's (host) work; this call does the copies.
+ *
+ *  k_cache, v_cache [num_blocks, block_size, Hkv, d] pools, written in place
+ *  src_blocks, dst_blocks int32 [num_pairs] (device): block src_blocks[i] is
+ *        copied over block dst_blocks[i] in both pools, bit for bit
+ * Destinations must be distinct and no destination may be the source of
+ * another pair in the same call (the copies run concurrently). A pair with
+ * an id outside [0, num_blocks) raises PA_DEV_BAD_BLOCK and is skipped; a
+ * pair with src == dst is a no-op. Alignment: pools 16-byte aligned, the id
+ * arrays 4-byte aligned.
+ */
+PA_API int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_blocks,
+                          const int32_t* dst_blocks, int num_pairs, int block_size, int Hkv,
+                          int d, int num_blocks, pa_dtype dtype, int32_t* err_flag,
+                          void* stream);
+
+/*
  * attn_decode_paged -- one query per sequence, attending over every cached
  * key of that sequence through its block table (the query's own key
  * included; no causal mask is needed), optionally limited to the last

@@ -34,6 +34,7 @@ from .paged import (
     paged_slot,
     gather_paged,
     append_paged,
+    copy_blocks,
     decode_paged,
     prefill_paged,
 )
@@ -49,6 +50,7 @@ __all__ = [
     "paged_slot",
     "gather_paged",
     "append_paged",
+    "copy_blocks",
     "decode_paged",
     "prefill_paged",
     "kv_cache_bytes",

@@ -30,7 +30,8 @@ import numpy as np
 
 from .attention import _as_f64, sdpa
 
-__all__ = ["paged_slot", "gather_paged", "append_paged", "decode_paged", "prefill_paged"]
+__all__ = ["paged_slot", "gather_paged", "append_paged", "copy_blocks", "decode_paged",
+           "prefill_paged"]
 
 
 def paged_slot(block_table_row, position, block_size):
@@ -80,6 +81,23 @@ def append_paged(k_pool, v_pool, k_new, v_new, block_table, seq_lens, cu_new, bl
             blk, off = paged_slot(block_table[b], pos, block_size)
             k_out[blk, off] = k_new[i]
             v_out[blk, off] = v_new[i]
+    return k_out, v_out
+
+
+def copy_blocks(k_pool, v_pool, pairs):
+    """Copy-on-write's device step ("Module 09: Efficient Attention", section
+    "Sharing Blocks: Copy-on-Write"): copies of the pools in which block dst
+    holds block src's contents, for each (src, dst) pair; pairs whose ids
+    fall outside the pool, or with src == dst, change nothing. Byte copies,
+    so the GPU must match bit for bit."""
+    k_out = k_pool.clone() if hasattr(k_pool, "clone") else np.array(k_pool, copy=True)
+    v_out = v_pool.clone() if hasattr(v_pool, "clone") else np.array(v_pool, copy=True)
+    n = k_out.shape[0]
+    for src, dst in pairs:
+        src, dst = int(src), int(dst)
+        if 0 <= src < n and 0 <= dst < n and src != dst:
+            k_out[dst] = k_pool[src]
+            v_out[dst] = v_pool[src]
     return k_out, v_out
 
 

@@ -33,7 +33,8 @@ def declared_symbols():
 def test_header_declares_the_entry_points():
     syms = declared_symbols()
     for name in ("pa_attn_prefill", "pa_attn_prefill_paged", "pa_kv_append_paged",
-                 "pa_attn_decode_paged", "pa_decode_workspace_bytes", "pa_status_str"):
+                 "pa_copy_blocks", "pa_attn_decode_paged", "pa_decode_workspace_bytes",
+                 "pa_status_str"):
         assert name in syms
 
 
@@ -113,6 +114,21 @@ def test_append_host_validation(lib):
     assert _append(lib, kc=FAKE + 4) == PA_ERR_INVALID_ARG
     assert _append(lib, d=32) == PA_ERR_INVALID_ARG
     assert _append(lib, nb=0) == PA_ERR_INVALID_ARG
+
+
+def test_copy_blocks_host_validation(lib):
+    def cb(**kw):
+        a = dict(kc=FAKE, vc=FAKE, src=FAKE, dst=FAKE, n=3, bs=16, Hkv=2, d=64, nb=8, dt=0,
+                 err=None, stream=None)
+        a.update(kw)
+        return lib.pa_copy_blocks(a["kc"], a["vc"], a["src"], a["dst"], a["n"], a["bs"],
+                                  a["Hkv"], a["d"], a["nb"], a["dt"], a["err"], a["stream"])
+    assert cb(src=None) == PA_ERR_INVALID_ARG
+    assert cb(kc=FAKE + 8) == PA_ERR_INVALID_ARG
+    assert cb(d=80) == PA_ERR_INVALID_ARG
+    assert cb(nb=0) == PA_ERR_INVALID_ARG
+    assert cb(n=-1) == PA_ERR_INVALID_ARG
+    assert cb(n=0) == PA_OK                                      # nothing to copy, no launch
 
 
 def _decode(lib, **kw):

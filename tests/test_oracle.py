@@ -455,6 +455,60 @@ def test_allocator_invariant():
         alloc.free(10_000)
 
 
+def test_cow_share_demo(golden):
+    """The notebook's sharing demo: sharing an 8-token prompt's 2 blocks with a
+    second sample uses no new block, and both tables start with the same
+    physical block."""
+    want = {k: int(v) for k, v in golden("cow_share_demo.txt")}
+    bs = want["block_size"]
+    tables = SequenceTables(BlockAllocator(want["num_blocks"]), bs)
+    prompt = tables.add_sequence()
+    tables.reserve(prompt, want["prompt_tokens"])
+    before = tables.allocator.num_used
+    sample = tables.share_prefix(prompt, blocks_needed(want["prompt_tokens"], bs))
+    assert before == want["blocks_used_before_sharing"]
+    assert tables.allocator.num_used == want["blocks_used_after_sharing"]
+    assert int(tables.tables[sample][0] == tables.tables[prompt][0]) == \
+        want["same_physical_prefix_block"]
+
+
+def test_cow_copies_only_the_written_shared_block():
+    """A 10-token prompt (blocks of 4: the third block is partly filled) is
+    shared whole; when the sharer appends, exactly the partly filled shared
+    block is copied, the full prefix blocks stay shared, and the prompt's own
+    table is untouched. Then the prompt appends too: its third block is no
+    longer shared, so nothing is copied."""
+    alloc = BlockAllocator(12)
+    tables = SequenceTables(alloc, 4)
+    src = tables.add_sequence()
+    tables.reserve(src, 10)
+    orig = list(tables.tables[src])
+    dst = tables.share_prefix(src, 3)
+    assert tables.lengths[dst] == 10 and alloc.num_used == 3
+    assert [alloc.refcount(b) for b in orig] == [2, 2, 2]
+    copies = tables.prepare_write(dst, 13)  # positions 10..12: block 2 (shared), block 3 (new)
+    assert copies == [(orig[2], tables.tables[dst][2])]
+    assert tables.tables[dst][:2] == orig[:2] and tables.tables[dst][2] != orig[2]
+    assert len(tables.tables[dst]) == 4 and tables.tables[src] == orig
+    assert [alloc.refcount(b) for b in orig] == [2, 2, 1]
+    assert tables.prepare_write(src, 12) == []
+    assert alloc.num_used + alloc.num_free == 12
+    # releasing the sharer frees only what nobody else holds
+    used = alloc.num_used
+    tables.release(dst)
+    assert alloc.num_used == used - 2 and [alloc.refcount(b) for b in orig] == [1, 1, 1]
+    tables.release(src)
+    assert alloc.num_used == 0
+
+
+def test_copy_blocks_oracle():
+    k = np.arange(6 * 2 * 3, dtype=np.float64).reshape(6, 2, 3)
+    v = -k
+    k2, v2 = oracle.copy_blocks(k, v, [(1, 4), (5, 0), (2, 99)])
+    assert (k2[4] == k[1]).all() and (v2[0] == v[5]).all()
+    assert (k2[[1, 2, 3, 5]] == k[[1, 2, 3, 5]]).all() and (k == np.arange(36).reshape(6, 2, 3)).all()
+
+
 def test_kv_bytes(golden):
     for name, layers, kvh, hd, b, n, want in golden("kv_bytes.txt"):
         got = oracle.kv_cache_bytes(int(layers), int(kvh), int(n), int(hd), int(b))
