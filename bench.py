@@ -56,7 +56,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixed_window4096",
                     choices=["mixed_window4096", "gqa_decode_llama3_70b", "mha_decode_gpt2",
-                             "gqa_prefill_llama3_8b", "chunked_prefill_llama3_8b"],
+                             "gqa_prefill_llama3_8b", "chunked_prefill_llama3_8b",
+                             "cow_copy_blocks_llama3_8b"],
                     help="other workloads time a single kernel family (profiling aid)")
     ap.add_argument("--only", choices=["prefill", "append", "decode"], default=None,
                     help="run only one phase of the mixed step (profiling aid)")
@@ -90,6 +91,7 @@ KERNEL_SOURCES = {
     "prefill_bf16": ("prefill_sm103.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
     "decode_bf16": ("decode_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
     "kv_append": ("append_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
+    "copy_blocks": ("copy_blocks.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
 }
 
 
@@ -274,7 +276,25 @@ class SingleStep:
         self.b = binding
         self.name = name
         self.err = binding.new_err_flag(device)
-        if name == "chunked_prefill_llama3_8b":
+        if name == "cow_copy_blocks_llama3_8b":
+            # copy-on-write: 2048 random (src, dst) pairs of Llama-3-8B-layout
+            # blocks (16 tokens x 8 KV heads x 128, bf16: 32 KB per pool)
+            nb, pairs = 8192, 2048
+            seed = inputs.WORKLOAD_SEEDS["cow_copy_blocks_llama3_8b"]
+            perm = torch.randperm(nb, generator=inputs.make_generator(seed))
+            dgen = inputs.make_generator(seed + 1, device)
+            self.w = {
+                "k_cache": inputs.randn((nb, 16, 8, 128), torch.bfloat16, dgen, device),
+                "v_cache": inputs.randn((nb, 16, 8, 128), torch.bfloat16, dgen, device),
+                "src": perm[:pairs].to(torch.int32).to(device),
+                "dst": perm[pairs:2 * pairs].to(torch.int32).to(device),
+            }
+            self.cbytes = 2.0 * 2 * pairs * 16 * 8 * 128 * 2  # K and V, read and written
+            self.flops = 0.0
+            self.dbytes = 0.0
+            self.phase = "copy"
+            self.launches = {"copy": 1}
+        elif name == "chunked_prefill_llama3_8b":
             w = inputs.chunked_prefill_llama3_8b(device)
             self.w = w
             self.out = torch.empty_like(w["q"])
@@ -310,7 +330,9 @@ class SingleStep:
 
     def run(self):
         w = self.w
-        if self.name == "chunked_prefill_llama3_8b":
+        if self.phase == "copy":
+            self.b.copy_blocks(w["k_cache"], w["v_cache"], w["src"], w["dst"], err_flag=self.err)
+        elif self.name == "chunked_prefill_llama3_8b":
             self.b.attn_prefill_paged(w["q"], w["k_cache"], w["v_cache"], w["block_table"],
                                       w["seq_lens"], w["cu_seqlens_q"], w["chunk"],
                                       out=self.out, lse=self.lse, err_flag=self.err)
@@ -504,12 +526,11 @@ def run_ours(args):
     phase_ms = {ph: sum(v) / len(v) for ph, v in times.items()}
     step_ms = sum(phase_ms.values())
     if world > 1:
-        t = torch.tensor([phase_ms.get(p, 0.0) for p in ("prefill", "append", "decode")] +
-                         [step_ms], device=dev)
+        names = ("prefill", "append", "decode", "copy")
+        t = torch.tensor([phase_ms.get(p, 0.0) for p in names] + [step_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        phase_ms = {p: float(t[i]) for i, p in enumerate(("prefill", "append", "decode"))
-                    if p in phase_ms}
-        step_ms = float(t[3])
+        phase_ms = {p: float(t[i]) for i, p in enumerate(names) if p in phase_ms}
+        step_ms = float(t[len(names)])
 
     # throughput per phase (whole job: all replicas' work over the slowest rank)
     phases_out = {}
@@ -521,6 +542,10 @@ def run_ours(args):
         gb = world * st.abytes / (phase_ms["append"] * 1e-3) / 1e9
         phases_out["append"] = {"ms": phase_ms["append"], "value": gb, "unit": "GB/s",
                                 "work": st.abytes, "launches": st.launches["append"]}
+    if "copy" in phase_ms:
+        gb = world * st.cbytes / (phase_ms["copy"] * 1e-3) / 1e9
+        phases_out["copy"] = {"ms": phase_ms["copy"], "value": gb, "unit": "GB/s",
+                              "work": st.cbytes, "launches": st.launches["copy"]}
     if "decode" in phase_ms:
         gb = world * st.dbytes / (phase_ms["decode"] * 1e-3) / 1e9
         phases_out["decode"] = {"ms": phase_ms["decode"], "value": gb, "unit": "GB/s",
@@ -540,7 +565,8 @@ def run_ours(args):
         r["frac"] = r["achieved"] / r["peak"]
         r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" \
             else "fallback (recipe)"
-        kname = {"prefill": "prefill_bf16", "append": "kv_append", "decode": "decode_bf16"}[ph]
+        kname = {"prefill": "prefill_bf16", "append": "kv_append", "decode": "decode_bf16",
+                 "copy": "copy_blocks"}[ph]
         r["traffic"] = recorded_traffic(kname, args.workload)
         r["kernel_share"] = phase_ms[ph] / step_ms
         roof[ph] = r
@@ -584,7 +610,8 @@ def run_ours(args):
         cfg.update({"l2": L2_NOTE})
     line = {
         "metric": METRIC if args.workload == "mixed_window4096" else
-        {"prefill": "causal prefill attention TFLOP/s", "decode": "paged decode KV-read GB/s"}[head],
+        {"prefill": "causal prefill attention TFLOP/s", "decode": "paged decode KV-read GB/s",
+         "copy": "copy-on-write block copy GB/s (read + written)"}[head],
         "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",

@@ -57,6 +57,7 @@ WORKLOAD_SEEDS = {
     "gqa_decode_llama3_70b": 1003,
     "mixed_window4096": 1004,
     "chunked_prefill_llama3_8b": 1005,
+    "cow_copy_blocks_llama3_8b": 1006,
 }
 
 
