@@ -695,7 +695,6 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         tmem_ld32(tO + 32 * c, o);
         tmem_wait_ld();
         if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
           const uint64_t inv2 = f2(inv, inv);
           uint32_t w[16];
 #pragma unroll
@@ -704,8 +703,9 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
             unf2(fmul2(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2), lo, hi);
             w[e] = pack_bf16(lo, hi);
           }
-#pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          // two 32-byte stores per 32 columns: whole sectors (rows are 256-B aligned)
+          st_global_v8(orow + 32 * c, w);
+          st_global_v8(orow + 32 * c + 16, w + 8);
         }
       }
       if (a.lse && live)
