@@ -171,10 +171,11 @@ __device__ __forceinline__ bool decode_unit(const PrefillArgs& a, int level, int
 // round-robin to the CTAs -- are all real work.
 struct Sched {
   const uint16_t* order;  // sequence of each rank
-  const uint16_t* nl;     // levels of each rank, non-increasing
+  const uint16_t* nl;     // levels of each rank (non-increasing unless seq_major)
   int nseq, npairs, nlev;
   bool compact;
-  int L, cum, cnt;        // compact walk: current level, indices below it, ranks that have it
+  bool seq_major;         // paged keys: rank by rank (longest cache first), not level by level
+  int L, cum, cnt;        // compact walk: current level (seq_major: rank), indices below it, ...
 
   __device__ __forceinline__ int count_gt(int lv) const {  // ranks with more than lv levels
     int lo = 0, hi = nseq;
@@ -185,7 +186,10 @@ struct Sched {
     return lo;
   }
   __device__ __forceinline__ void start() {
-    if (compact) {
+    if (compact && seq_major) {
+      L = 0;  // rank
+      cum = 0;
+    } else if (compact) {
       L = static_cast<int>(nl[0]) - 1;
       cum = 0;
       cnt = L >= 0 ? count_gt(L) : 0;
@@ -193,7 +197,18 @@ struct Sched {
   }
   // indices must be visited in increasing order
   __device__ __forceinline__ void map(int v, int& level, int& b, int& pair) {
-    if (compact) {
+    if (compact && seq_major) {
+      // a sequence's units (its levels, highest first, times the pairs) are
+      // consecutive, so the units in flight share one or two sequences' keys
+      while (v >= cum + static_cast<int>(nl[L]) * npairs) {
+        cum += static_cast<int>(nl[L]) * npairs;
+        ++L;
+      }
+      const int j = v - cum;
+      b = order[L];
+      level = static_cast<int>(nl[L]) - 1 - j / npairs;
+      pair = j % npairs;
+    } else if (compact) {
       while (v >= cum + cnt * npairs) {
         cum += cnt * npairs;
         --L;
@@ -277,10 +292,17 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
   if (a.compact) {
     uint16_t* tmp = reinterpret_cast<uint16_t*>(gb + C::OFF_RING);  // the ring is still unused
     if (threadIdx.x == 0) *s_total = 0;
-    for (int b = threadIdx.x; b < a.B; b += kThreads) {
+    // levels of sequence b; the sort key is the level count, or with paged
+    // keys the cache length in blocks (the work grows with the cached prefix)
+    auto levels = [&](int b) {
       const int len = max(0, min(a.cu_seqlens[b + 1] - a.cu_seqlens[b], a.max_seqlen));
       const int nqt = (len + BM - 1) / BM;
-      tmp[b] = static_cast<uint16_t>(a.pair_heads ? nqt : (nqt + 1) >> 1);
+      return a.pair_heads ? nqt : (nqt + 1) >> 1;
+    };
+    for (int b = threadIdx.x; b < a.B; b += kThreads) {
+      int key = levels(b);
+      if (a.table) key = min(65535, (min(max(a.seq_lens_k[b], 0), a.max_blocks * 16) + 15) / 16);
+      tmp[b] = static_cast<uint16_t>(key);
     }
     __syncthreads();
     int part = 0;
@@ -291,9 +313,10 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         const int n2 = tmp[b2];
         rank += (n2 > n) || (n2 == n && b2 < b);
       }
+      const int nl = levels(b);
       s_order[rank] = static_cast<uint16_t>(b);
-      s_nl[rank] = static_cast<uint16_t>(n);
-      part += n;
+      s_nl[rank] = static_cast<uint16_t>(nl);
+      part += nl;
     }
     __syncthreads();  // *s_total zeroed and every rank of tmp read
     if (part) atomicAdd(s_total, part * npairs);
@@ -333,6 +356,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
   sched.npairs = npairs;
   sched.nlev = a.pair_heads ? (a.max_seqlen + BM - 1) / BM : ((a.max_seqlen + BM - 1) / BM + 1) / 2;
   sched.compact = a.compact != 0;
+  sched.seq_major = a.table != nullptr;
   sched.start();
   const int n_units = a.compact ? *s_total : a.n_units;
 
