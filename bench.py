@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--workload", default="mixed_window4096",
                     choices=["mixed_window4096", "gqa_decode_llama3_70b", "mha_decode_gpt2",
                              "gqa_prefill_llama3_8b", "chunked_prefill_llama3_8b",
-                             "cow_copy_blocks_llama3_8b"],
+                             "cow_copy_blocks_llama3_8b", "gqa_prefill_backward_llama3_8b"],
                     help="other workloads time a single kernel family (profiling aid)")
     ap.add_argument("--only", choices=["prefill", "append", "decode"], default=None,
                     help="run only one phase of the mixed step (profiling aid)")
@@ -92,6 +92,7 @@ KERNEL_SOURCES = {
     "decode_bf16": ("decode_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
     "kv_append": ("append_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
     "copy_blocks": ("copy_blocks.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
+    "prefill_backward": ("prefill_bwd.cu", "bwd_kernels.h", "pa_ptx.cuh", "capi.cu"),
 }
 
 
@@ -188,6 +189,12 @@ def prefill_flops(lengths, hq, d, window):
         else:
             pairs += n * (n + 1) // 2
     return 4.0 * d * hq * pairs
+
+
+def backward_flops(lengths, hq, d, window):
+    """10*d FLOPs per visible (query, key) pair and query head: five
+    products of 2*d each (S and dP recomputed, dV, dK, dQ)."""
+    return 2.5 * prefill_flops(lengths, hq, d, window)
 
 
 def chunked_prefill_flops(prefixes, chunk, hq, d):
@@ -303,6 +310,26 @@ class SingleStep:
             self.dbytes = 0.0
             self.phase = "prefill"
             self.launches = {"prefill": 1}
+        elif name == "gqa_prefill_backward_llama3_8b":
+            # gradients of the Llama-3-8B-shaped prefill: the forward pass runs
+            # once (untimed) for O and the LSE; dO is seeded noise
+            w = inputs.gqa_prefill_llama3_8b(device)
+            self.w = w
+            gen = inputs.make_generator(inputs.WORKLOAD_SEEDS["gqa_prefill_llama3_8b"] + 9, device)
+            self.dout = inputs.randn(w["q"].shape, torch.bfloat16, gen, device)
+            self.out, self.lse = binding.attn_prefill(w["q"], w["k"], w["v"], causal=True,
+                                                      cu_seqlens=w["cu_seqlens"],
+                                                      max_seqlen=w["max_seqlen"])
+            self.dq = torch.empty_like(w["q"])
+            self.dk = torch.empty_like(w["k"])
+            self.dv = torch.empty_like(w["v"])
+            need = binding.prefill_backward_workspace_bytes(w["q"].shape[0], w["hq"], w["d"])
+            self.ws = torch.empty(need, dtype=torch.uint8, device=device)
+            self.flops = backward_flops(w["lengths"], w["hq"], w["d"], 0)
+            self.dbytes = 0.0
+            self.phase = "backward"
+            # row dot products, main kernel, dQ conversion (plus a memset)
+            self.launches = {"backward": 3}
         elif name == "gqa_prefill_llama3_8b":
             w = inputs.gqa_prefill_llama3_8b(device)
             self.w = w
@@ -332,6 +359,11 @@ class SingleStep:
         w = self.w
         if self.phase == "copy":
             self.b.copy_blocks(w["k_cache"], w["v_cache"], w["src"], w["dst"], err_flag=self.err)
+        elif self.phase == "backward":
+            self.b.attn_prefill_backward(w["q"], w["k"], w["v"], self.out, self.dout, self.lse,
+                                         causal=True, cu_seqlens=w["cu_seqlens"],
+                                         max_seqlen=w["max_seqlen"], dq=self.dq, dk=self.dk,
+                                         dv=self.dv, workspace=self.ws, err_flag=self.err)
         elif self.name == "chunked_prefill_llama3_8b":
             self.b.attn_prefill_paged(w["q"], w["k_cache"], w["v_cache"], w["block_table"],
                                       w["seq_lens"], w["cu_seqlens_q"], w["chunk"],
@@ -526,7 +558,7 @@ def run_ours(args):
     phase_ms = {ph: sum(v) / len(v) for ph, v in times.items()}
     step_ms = sum(phase_ms.values())
     if world > 1:
-        names = ("prefill", "append", "decode", "copy")
+        names = ("prefill", "append", "decode", "copy", "backward")
         t = torch.tensor([phase_ms.get(p, 0.0) for p in names] + [step_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         phase_ms = {p: float(t[i]) for i, p in enumerate(names) if p in phase_ms}
@@ -538,6 +570,10 @@ def run_ours(args):
         tf = world * st.flops / (phase_ms["prefill"] * 1e-3) / 1e12
         phases_out["prefill"] = {"ms": phase_ms["prefill"], "value": tf, "unit": "TFLOP/s",
                                  "work": st.flops, "launches": st.launches["prefill"]}
+    if "backward" in phase_ms:
+        tf = world * st.flops / (phase_ms["backward"] * 1e-3) / 1e12
+        phases_out["backward"] = {"ms": phase_ms["backward"], "value": tf, "unit": "TFLOP/s",
+                                  "work": st.flops, "launches": st.launches["backward"]}
     if "append" in phase_ms:
         gb = world * st.abytes / (phase_ms["append"] * 1e-3) / 1e9
         phases_out["append"] = {"ms": phase_ms["append"], "value": gb, "unit": "GB/s",
@@ -555,7 +591,7 @@ def run_ours(args):
     dom = max(phase_ms, key=phase_ms.get)
     roof = {}
     for ph, info in phases_out.items():
-        if ph == "prefill":
+        if ph in ("prefill", "backward"):
             peak = peaks["bf16_tflops"]
             r = {"bound": "tensor", "achieved": info["value"] / world, "peak": peak,
                  "unit": "TFLOP/s"}
@@ -566,7 +602,7 @@ def run_ours(args):
         r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" \
             else "fallback (recipe)"
         kname = {"prefill": "prefill_bf16", "append": "kv_append", "decode": "decode_bf16",
-                 "copy": "copy_blocks"}[ph]
+                 "copy": "copy_blocks", "backward": "prefill_backward"}[ph]
         r["traffic"] = recorded_traffic(kname, args.workload)
         r["kernel_share"] = phase_ms[ph] / step_ms
         roof[ph] = r
@@ -611,6 +647,7 @@ def run_ours(args):
     line = {
         "metric": METRIC if args.workload == "mixed_window4096" else
         {"prefill": "causal prefill attention TFLOP/s", "decode": "paged decode KV-read GB/s",
+         "backward": "causal prefill attention backward TFLOP/s (10*d per visible pair)",
          "copy": "copy-on-write block copy GB/s (read + written)"}[head],
         "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,

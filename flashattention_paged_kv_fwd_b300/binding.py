@@ -74,6 +74,12 @@ def load_library():
     lib.pa_attn_decode_paged.restype = i32
     lib.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.pa_decode_workspace_bytes.restype = sz
+    lib.pa_attn_prefill_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                             i32, i32, vp, i32, i32, i32, f32, vp, sz, i32, vp,
+                                             vp]
+    lib.pa_attn_prefill_backward.restype = i32
+    lib.pa_attn_prefill_backward_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.pa_attn_prefill_backward_workspace_bytes.restype = sz
     _LIB = lib
     return lib
 
@@ -166,6 +172,67 @@ def attn_prefill(q, k, v, *, causal=True, window=0, scale=None, cu_seqlens=None,
                              _stream(stream))
     _check(st, "attn_prefill")
     return out, lse
+
+
+def prefill_backward_workspace_bytes(total_tokens, hq, d):
+    """Workspace bytes attn_prefill_backward needs for ``total_tokens`` tokens."""
+    return int(load_library().pa_attn_prefill_backward_workspace_bytes(int(total_tokens), int(hq),
+                                                                        int(d)))
+
+
+def attn_prefill_backward(q, k, v, o, dout, lse, *, causal=True, window=0, scale=None,
+                          cu_seqlens=None, max_seqlen=None, dq=None, dk=None, dv=None,
+                          workspace=None, err_flag=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_prefill's output for the upstream
+    gradient ``dout`` (bf16, shaped like q), given that call's o and lse.
+
+    Same layouts and sequence addressing as :func:`attn_prefill`. dk and dv
+    hold each KV head's sum over its query heads. Rows of k / v that belong
+    to no sequence are not written; such rows of dq are zero. ``workspace``
+    (uint8, >= attn_prefill_backward_workspace_bytes) is allocated when
+    not given.
+    """
+    lib = load_library()
+    _need(q.dtype == torch.bfloat16, "the backward pass takes bfloat16 tensors")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _cuda_contig(name, t, q.dtype)
+    _need(o.shape == q.shape and dout.shape == q.shape, "o and dout must be shaped like q")
+    d = q.shape[-1]
+    hq, hkv = q.shape[-2], k.shape[-2]
+    if cu_seqlens is None:
+        _need(q.dim() == 4 and k.dim() == 4 and v.shape == k.shape, "q must be [B, N, Hq, d]")
+        B, N = q.shape[0], q.shape[1]
+        _need(k.shape[:2] == (B, N), "k/v must be [B, N, Hkv, d]")
+        T = B * N
+        n_arg, msl = N, N
+    else:
+        _cuda_contig("cu_seqlens", cu_seqlens, torch.int32)
+        _need(q.dim() == 3 and k.dim() == 3 and v.shape == k.shape, "q must be [T, Hq, d]")
+        _need(max_seqlen is not None, "max_seqlen is required with cu_seqlens")
+        B = cu_seqlens.numel() - 1
+        T = q.shape[0]
+        _need(k.shape[0] == T, "k/v must have the same token count as q")
+        n_arg, msl = T, int(max_seqlen)
+    _need(k.shape[-1] == d, "head dims differ")
+    _cuda_contig("lse", lse, torch.float32)
+    _need(lse.shape == (hq, T), "lse must be [Hq, T]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _cuda_contig(name, t, q.dtype)
+        _need(t.shape == ref.shape, f"{name} must be shaped like its input")
+    need = prefill_backward_workspace_bytes(T, hq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _cuda_contig("workspace", workspace, torch.uint8)
+    st = lib.pa_attn_prefill_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+        B, hq, hkv, n_arg, d, _ptr(cu_seqlens), msl, 1 if causal else 0, int(window or 0),
+        float(scale or 0.0), _ptr(workspace), workspace.numel(), _DTYPES[q.dtype],
+        _ptr(err_flag), _stream(stream))
+    _check(st, "attn_prefill_backward")
+    return dq, dk, dv
 
 
 def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, seq_lens, *, cu_new=None,

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/pagedattn.h"
+#include "bwd_kernels.h"
 #include "pa_kernels.h"
 
 namespace {
@@ -94,9 +95,12 @@ bool encode_pool(CUtensorMap* m, const void* ptr, int d, int heads, int block_si
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+double softmax_scale(float scale, int d) {
+  return scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(d));
+}
+
 float scale_log2(float scale, int d) {
-  const double s = scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(d));
-  return static_cast<float>(s * 1.4426950408889634074);  // * log2(e)
+  return static_cast<float>(softmax_scale(scale, d) * 1.4426950408889634074);  // * log2(e)
 }
 
 }  // namespace
@@ -122,7 +126,9 @@ int pa_attn_prefill(const void* q, const void* k, const void* v, void* o, float*
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || N < 0 || Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return PA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o) return PA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+  // the bf16 epilogue writes O in 32-byte pieces
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(o, dtype == PA_BF16 ? 32 : 16))
     return PA_ERR_INVALID_ARG;
   if (lse && !aligned(lse, 4)) return PA_ERR_INVALID_ARG;
   if (err_flag && !aligned(err_flag, 4)) return PA_ERR_INVALID_ARG;
@@ -169,7 +175,7 @@ int pa_attn_prefill_paged(const void* q, const void* k_cache, const void* v_cach
     return PA_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !cu_seqlens_q || !o)
     return PA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 32) ||
       !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(cu_seqlens_q, 4) ||
       (lse && !aligned(lse, 4)) || (err_flag && !aligned(err_flag, 4)))
     return PA_ERR_INVALID_ARG;
@@ -190,6 +196,57 @@ int pa_attn_prefill_paged(const void* q, const void* k_cache, const void* v_cach
     return PA_ERR_CUDA;
   const cudaError_t e =
       pa::launch_prefill_bf16(a, qm, km, vm, sm_count(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_attn_prefill_backward_workspace_bytes(int total_tokens, int Hq, int d) {
+  if (total_tokens < 0 || Hq <= 0 || (d != 64 && d != 128)) return 0;
+  return pa::backward_workspace_bytes(total_tokens, Hq, d);
+}
+
+int pa_attn_prefill_backward(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             int B, int Hq, int Hkv, int N, int d, const int32_t* cu_seqlens,
+                             int max_seqlen, int causal, int window, float scale,
+                             void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                             int32_t* err_flag, void* stream) {
+  if (!valid_dtype(dtype)) return PA_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || N < 0 || Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (window > 0 && !causal) return PA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return PA_ERR_INVALID_ARG;
+  // dK / dV rows are written in 32-byte pieces, dQ in 16-byte pieces
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dout, 16) || !aligned(lse, 4) || !aligned(dq, 16) || !aligned(dk, 32) ||
+      !aligned(dv, 32) || (err_flag && !aligned(err_flag, 4)))
+    return PA_ERR_INVALID_ARG;
+  if (cu_seqlens && (max_seqlen < 0 || !aligned(cu_seqlens, 4))) return PA_ERR_INVALID_ARG;
+  const long long T = cu_seqlens ? static_cast<long long>(N) : static_cast<long long>(B) * N;
+  if (T > 0x7FFFFFFFLL) return PA_ERR_INVALID_ARG;
+  const int msl = cu_seqlens ? max_seqlen : N;
+  if (T == 0 || msl == 0) return PA_OK;
+  const size_t need = pa::backward_workspace_bytes(T, Hq, d);
+  if (!workspace || workspace_bytes < need) return PA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+
+  pa::BackwardArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse = lse;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.dq_acc = static_cast<float*>(workspace);
+  a.dvec = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                    (static_cast<size_t>(T) * Hq * d * 4 + 255) / 256 * 256);
+  a.cu_seqlens = cu_seqlens; a.err = err_flag;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.N = N; a.T = static_cast<int>(T); a.d = d;
+  a.max_seqlen = msl; a.causal = causal ? 1 : 0; a.window = window > 0 ? window : 0;
+  a.scale_log2 = scale_log2(scale, d);
+  a.scale = static_cast<float>(softmax_scale(scale, d));
+  CUtensorMap qm, km, vm, dom;
+  if (!encode_3d(&qm, q, d, Hq, T, 128) || !encode_3d(&km, k, d, Hkv, T, 128) ||
+      !encode_3d(&vm, v, d, Hkv, T, 128) || !encode_3d(&dom, dout, d, Hq, T, 128))
+    return PA_ERR_CUDA;
+  const cudaError_t e = pa::launch_prefill_backward_bf16(a, qm, km, vm, dom, sm_count(),
+                                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

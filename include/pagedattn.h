@@ -104,7 +104,8 @@ PA_API const char* pa_status_str(int status);
  *  causal      1 = causal, 0 = every query sees every key of its sequence
  *  window      <= 0: none; > 0: sliding window W (requires causal)
  *  scale       <= 0: 1/sqrt(d)
- * Alignment: q, k, v, o 16-byte aligned; lse 4-byte aligned.
+ * Alignment: q, k, v 16-byte aligned; o 32-byte aligned for bf16 (16 for
+ * f32); lse 4-byte aligned.
  */
 PA_API int pa_attn_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                     int Hq, int Hkv, int N, int d, const int32_t* cu_seqlens, int max_seqlen,
@@ -138,8 +139,8 @@ PA_API int pa_attn_prefill(const void* q, const void* k, const void* v, void* o,
  *  otherwise). causal / window / scale as in attn_prefill.
  * Slots of a block past a sequence's keys may hold anything (even NaN): they
  * are never used. A block id outside [0, num_blocks) raises PA_DEV_BAD_BLOCK
- * and that block is skipped. Alignment: q, pools, o 16-byte aligned; int32
- * arrays and lse 4-byte aligned.
+ * and that block is skipped. Alignment: q, pools 16-byte aligned; o 32-byte
+ * aligned; int32 arrays and lse 4-byte aligned.
  */
 PA_API int pa_attn_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_table, int max_blocks_per_seq,
@@ -148,6 +149,47 @@ PA_API int pa_attn_prefill_paged(const void* q, const void* k_cache, const void*
                                  int Hq, int Hkv, int d, int block_size, int num_blocks,
                                  int causal, int window, float scale, pa_dtype dtype,
                                  int32_t* err_flag, void* stream);
+
+/*
+ * attn_prefill_backward -- gradients of attn_prefill's output: given dO =
+ * dL/dO, returns dQ, dK, dV. "Cache KV, atención flash y optimización de la
+ * inferencia", section "La atención de flash el truco de la balsa": the
+ * backward pass recomputes the forward values (the scores and P) from Q, K
+ * and the saved per-row LSE instead of storing the attention matrix. The
+ * gradients are the chain rule through O = softmax(S) V, S = scale Q K^T:
+ *   P = exp(S - lse), dV = P^T dO, dP = dO V^T, D_i = sum_c dO_ic O_ic,
+ *   dS = P (dP - D), dQ = scale dS K, dK = scale dS^T Q,
+ * with masked (invisible) pairs contributing nothing; dK and dV of a KV head
+ * are summed over the query heads that read it.
+ *
+ *  q, o, dout [T, Hq, d] bf16: the forward call's queries and output, and
+ *             the upstream gradient
+ *  k, v       [T, Hkv, d] bf16
+ *  lse        [Hq, T] float32: the forward call's LSE (natural log)
+ *  dq [T, Hq, d], dk, dv [T, Hkv, d] bf16 outputs (must not alias inputs).
+ *             Rows of dq outside every sequence are set to zero; such rows
+ *             of dk / dv are not written.
+ *  B, N, cu_seqlens, max_seqlen, causal, window, scale: as in attn_prefill,
+ *             and the same values the forward call used
+ *  workspace  device buffer of >= pa_attn_prefill_backward_workspace_bytes
+ *             bytes, 256-byte aligned, owned by the caller, unused after the
+ *             stream reaches the end of this call (fp32 dQ accumulator and
+ *             the D vector)
+ * dtype must be PA_BF16 (PA_ERR_UNSUPPORTED otherwise); d is 64 or 128.
+ * Alignment: q, k, v, o, dout, dq 16-byte aligned; dk, dv 32-byte aligned;
+ * lse 4-byte aligned. Errors: PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED /
+ * PA_ERR_WORKSPACE before any CUDA call; PA_DEV_TIMEOUT in err_flag if a
+ * bounded wait of the main kernel gave up.
+ */
+PA_API size_t pa_attn_prefill_backward_workspace_bytes(int total_tokens, int Hq, int d);
+
+PA_API int pa_attn_prefill_backward(const void* q, const void* k, const void* v, const void* o,
+                                    const void* dout, const float* lse, void* dq, void* dk,
+                                    void* dv, int B, int Hq, int Hkv, int N, int d,
+                                    const int32_t* cu_seqlens, int max_seqlen, int causal,
+                                    int window, float scale, void* workspace,
+                                    size_t workspace_bytes, pa_dtype dtype, int32_t* err_flag,
+                                    void* stream);
 
 /*
  * kv_append_paged -- write new tokens' keys and values into the paged pools.

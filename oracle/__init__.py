@@ -27,6 +27,9 @@ from .attention import (
     sdpa,
     sdpa_rows,
     sdpa_varlen,
+    sdpa_backward,
+    sdpa_backward_varlen,
+    sdpa_backward_sampled,
     online_softmax_attention,
     merge_splits,
 )
@@ -45,6 +48,9 @@ __all__ = [
     "sdpa",
     "sdpa_rows",
     "sdpa_varlen",
+    "sdpa_backward",
+    "sdpa_backward_varlen",
+    "sdpa_backward_sampled",
     "online_softmax_attention",
     "merge_splits",
     "paged_slot",

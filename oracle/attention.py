@@ -42,6 +42,9 @@ __all__ = [
     "sdpa",
     "sdpa_rows",
     "sdpa_varlen",
+    "sdpa_backward",
+    "sdpa_backward_varlen",
+    "sdpa_backward_sampled",
     "online_softmax_attention",
     "merge_splits",
 ]
@@ -188,6 +191,116 @@ def sdpa_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, causal, window=0, scale=
         o[q0:q1] = ob
         lse[:, q0:q1] = lb
     return o, lse
+
+
+def sdpa_backward(q, k, v, dout, *, causal, window=0, scale=None):
+    """Gradients of :func:`sdpa`'s output for ONE sequence, in fp64.
+
+    Given dL/dO = dout [len_q, Hq, d], returns (dq [len_q, Hq, d],
+    dk [len_k, Hkv, d], dv [len_k, Hkv, d]) of L through O = softmax(S) V with
+    S = scale * Q K^T (masked keys excluded). Written from the chain rule of
+    those two steps ("Cache KV, atención flash ...", section "La atención de
+    flash el truco de la balsa": the backward pass recomputes S and P from Q,
+    K and the saved row statistics instead of storing P):
+        dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij = sum_c dO_ic O_ic,
+        dS = P * (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
+    Query heads of one KV group add their dK, dV into that group's KV head.
+    """
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    len_q, hq, d = q.shape
+    len_k, hkv, _ = k.shape
+    _check_heads(hq, hkv)
+    if scale is None:
+        scale = default_scale(d)
+    allowed = attention_mask(len_q, len_k, causal, window)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    has_key = allowed.any(axis=1)
+    for h in range(hq):
+        g = kv_head_of(h, hq, hkv)
+        s = np.where(allowed, scale * (q[:, h, :] @ k[:, g, :].T), -np.inf)
+        p = np.zeros_like(s)
+        if has_key.any():
+            sv = s[has_key]
+            e = np.exp(sv - sv.max(axis=1, keepdims=True))
+            p[has_key] = e / e.sum(axis=1, keepdims=True)
+        o = p @ v[:, g, :]
+        do = dout[:, h, :]
+        dv[:, g, :] += p.T @ do
+        dp = do @ v[:, g, :].T
+        drow = (do * o).sum(axis=1, keepdims=True)
+        ds = p * (dp - drow)
+        dq[:, h, :] = scale * (ds @ k[:, g, :])
+        dk[:, g, :] += scale * (ds.T @ q[:, h, :])
+    return dq, dk, dv
+
+
+def sdpa_backward_varlen(q, k, v, dout, cu_seqlens, *, causal, window=0, scale=None):
+    """:func:`sdpa_backward` of packed sequences (Lq = Lk per sequence)."""
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(len(cu_seqlens) - 1):
+        a, e = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        if e == a:
+            continue
+        dq[a:e], dk[a:e], dv[a:e] = sdpa_backward(q[a:e], k[a:e], v[a:e], dout[a:e],
+                                                  causal=causal, window=window, scale=scale)
+    return dq, dk, dv
+
+
+def sdpa_backward_sampled(q, k, v, dout, kv_head, q_rows, k_rows, *, causal, window=0,
+                          scale=None, chunk=1024):
+    """Selected entries of :func:`sdpa_backward` for ONE (long) sequence.
+
+    Returns (dq [len(q_rows), G, d] for the G query heads of ``kv_head``,
+    dk [len(k_rows), d], dv [len(k_rows), d] of ``kv_head``), the same
+    formulas evaluated only where asked. The score matrix is formed ``chunk``
+    query rows at a time to get every row's LSE and D (dK and dV of one key
+    need P and D of every query that sees it); then
+        dq_i = scale * sum_j P_ij (dP_ij - D_i) k_j,
+        dv_j = sum_i P_ij dO_i,  dk_j = scale * sum_i P_ij (dP_ij - D_i) q_i.
+    """
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    len_q, hq, d = q.shape
+    len_k, hkv, _ = k.shape
+    _check_heads(hq, hkv)
+    if scale is None:
+        scale = default_scale(d)
+    heads = [h for h in range(hq) if kv_head_of(h, hq, hkv) == kv_head]
+    kg, vg = k[:, kv_head, :], v[:, kv_head, :]
+    pos = query_position(np.arange(len_q), len_q, len_k)
+    keys = np.arange(len_k)
+    dq = np.zeros((len(q_rows), len(heads), d))
+    dk = np.zeros((len(k_rows), d))
+    dv = np.zeros((len(k_rows), d))
+    for hi, h in enumerate(heads):
+        qh, doh = q[:, h, :], dout[:, h, :]
+        lse = np.full(len_q, -np.inf)
+        drow = np.zeros(len_q)
+        for r0 in range(0, len_q, chunk):
+            r1 = min(len_q, r0 + chunk)
+            allowed = visible(pos[r0:r1, None], keys[None, :], causal, window)
+            s = np.where(allowed, scale * (qh[r0:r1] @ kg.T), -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            ok = np.isfinite(m[:, 0])
+            e = np.where(allowed, np.exp(s - np.where(np.isfinite(m), m, 0.0)), 0.0)
+            l = e.sum(axis=1)
+            lse[r0:r1] = np.where(ok, m[:, 0] + np.log(np.where(ok, l, 1.0)), -np.inf)
+            o = (e / np.where(ok, l, 1.0)[:, None]) @ vg
+            drow[r0:r1] = (doh[r0:r1] * o).sum(axis=1)
+        for n, i in enumerate(q_rows):
+            allowed = visible(pos[i], keys, causal, window)
+            p = np.where(allowed, np.exp(np.where(allowed, scale * (kg @ qh[i]), 0.0) - lse[i]), 0.0)
+            ds = p * (vg @ doh[i] - drow[i])
+            dq[n, hi] = scale * (ds @ kg)
+        for n, j in enumerate(k_rows):
+            allowed = visible(pos, j, causal, window)
+            p = np.where(allowed, np.exp(np.where(allowed, scale * (qh @ kg[j]), 0.0) - lse), 0.0)
+            dv[n] += p @ doh
+            ds = p * (doh @ vg[j] - drow)
+            dk[n] += scale * (ds @ qh)
+    return dq, dk, dv
 
 
 def online_softmax_attention(q, k, v, block, *, scale=None):

@@ -34,6 +34,7 @@ def test_header_declares_the_entry_points():
     syms = declared_symbols()
     for name in ("pa_attn_prefill", "pa_attn_prefill_paged", "pa_kv_append_paged",
                  "pa_copy_blocks", "pa_attn_decode_paged", "pa_decode_workspace_bytes",
+                 "pa_attn_prefill_backward", "pa_attn_prefill_backward_workspace_bytes",
                  "pa_status_str"):
         assert name in syms
 
@@ -74,6 +75,38 @@ def test_prefill_host_validation(lib):
     assert _prefill(lib, dt=7) == PA_ERR_INVALID_ARG
     assert _prefill(lib, causal=0, window=8) == PA_ERR_UNSUPPORTED
     assert _prefill(lib, N=0) == PA_OK                            # nothing to do, no launch
+    assert _prefill(lib, o=FAKE + 16) == PA_ERR_INVALID_ARG       # bf16 O: 32-byte alignment
+    assert _prefill(lib, o=FAKE + 16, dt=1, N=0) == PA_OK         # f32 O: 16 bytes suffice
+
+
+def _backward(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1,
+             Hq=4, Hkv=2, N=16, d=64, cu=None, msl=0, causal=1, window=0, scale=0.0, ws=FAKE,
+             wsb=1 << 30, dt=0, err=None, stream=None)
+    a.update(kw)
+    return lib.pa_attn_prefill_backward(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"],
+                                        a["dq"], a["dk"], a["dv"], a["B"], a["Hq"], a["Hkv"],
+                                        a["N"], a["d"], a["cu"], a["msl"], a["causal"],
+                                        a["window"], a["scale"], a["ws"], a["wsb"], a["dt"],
+                                        a["err"], a["stream"])
+
+
+def test_backward_host_validation(lib):
+    assert _backward(lib, Hq=6, Hkv=4) == PA_ERR_INVALID_ARG
+    assert _backward(lib, d=96) == PA_ERR_INVALID_ARG
+    assert _backward(lib, do=None) == PA_ERR_INVALID_ARG           # every tensor required
+    assert _backward(lib, lse=None) == PA_ERR_INVALID_ARG
+    assert _backward(lib, dk=FAKE + 16) == PA_ERR_INVALID_ARG      # dK / dV: 32-byte alignment
+    assert _backward(lib, dq=FAKE + 8) == PA_ERR_INVALID_ARG
+    assert _backward(lib, dt=1) == PA_ERR_UNSUPPORTED               # bf16 only
+    assert _backward(lib, causal=0, window=8) == PA_ERR_UNSUPPORTED
+    assert _backward(lib, ws=None) == PA_ERR_WORKSPACE
+    assert _backward(lib, wsb=100) == PA_ERR_WORKSPACE
+    assert _backward(lib, ws=FAKE + 16) == PA_ERR_INVALID_ARG      # workspace 256-byte aligned
+    assert _backward(lib, N=0, ws=None) == PA_OK                   # nothing to do, no launch
+    need = lib.pa_attn_prefill_backward_workspace_bytes(100, 4, 64)
+    assert need == (100 * 4 * 64 * 4 + 255) // 256 * 256 + (100 * 4 * 4 + 255) // 256 * 256
+    assert lib.pa_attn_prefill_backward_workspace_bytes(100, 4, 96) == 0
 
 
 def _prefill_paged(lib, **kw):
@@ -97,6 +130,7 @@ def test_prefill_paged_host_validation(lib):
     assert _prefill_paged(lib, dt=1) == PA_ERR_UNSUPPORTED           # bf16 only
     assert _prefill_paged(lib, causal=0, window=8) == PA_ERR_UNSUPPORTED
     assert _prefill_paged(lib, tq=0) == PA_OK                       # nothing to do, no launch
+    assert _prefill_paged(lib, o=FAKE + 16) == PA_ERR_INVALID_ARG   # O: 32-byte alignment
 
 
 def _append(lib, **kw):

@@ -509,6 +509,98 @@ def test_copy_blocks_oracle():
     assert (k2[[1, 2, 3, 5]] == k[[1, 2, 3, 5]]).all() and (k == np.arange(36).reshape(6, 2, 3)).all()
 
 
+def pin_backward_vs_autograd():
+    """Gradients against PyTorch autograd through its fp64 CPU
+    scaled_dot_product_attention (explicit mask, enable_gqa)."""
+    worst = 0.0
+    seed = 200
+    for (n, hq, hkv, d, causal, window) in [(11, 4, 2, 8, True, 0), (9, 3, 3, 16, False, 0),
+                                            (13, 4, 1, 8, True, 5)]:
+        q, k, v, do = (_rand(s, seed + i) for i, s in enumerate(
+            [(n, hq, d), (n, hkv, d), (n, hkv, d), (n, hq, d)]))
+        seed += 4
+        dq, dk, dv = oracle.sdpa_backward(q, k, v, do, causal=causal, window=window)
+        tq, tk, tv = (torch.tensor(x.transpose(1, 0, 2)[None], requires_grad=True)
+                      for x in (q, k, v))
+        mask = torch.from_numpy(oracle.attention_mask(n, n, causal, window))
+        o = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, enable_gqa=hq != hkv)
+        o.backward(torch.from_numpy(do.transpose(1, 0, 2)[None].copy()))
+        for mine, theirs in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+            worst = max(worst, float(np.abs(mine - theirs[0].numpy().transpose(1, 0, 2)).max()))
+    return worst
+
+
+def test_backward_matches_autograd():
+    assert pin_backward_vs_autograd() <= 1e-10
+
+
+def test_backward_finite_differences():
+    """Central differences of L = sum(dO * O) on a tiny GQA case."""
+    n, hq, hkv, d = 5, 2, 1, 4
+    q, k, v, do = (_rand(s, 300 + i) for i, s in enumerate(
+        [(n, hq, d), (n, hkv, d), (n, hkv, d), (n, hq, d)]))
+    dq, dk, dv = oracle.sdpa_backward(q, k, v, do, causal=True)
+    eps = 1e-6
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.sdpa(qq, kk, vv, causal=True)
+        return float((o * do).sum())
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        for idx in [(0, 0, 0), (2, 0, 3), (4, x.shape[1] - 1, 1)]:
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [xp if y is x else y for y in (q, k, v)]
+            args_m = [xm if y is x else y for y in (q, k, v)]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, g[idx])
+
+
+def test_backward_varlen_is_per_sequence():
+    lens = [3, 0, 7]
+    cu = np.cumsum([0] + lens)
+    q, k, v, do = (_rand(s, 310 + i) for i, s in enumerate(
+        [(cu[-1], 4, 8), (cu[-1], 2, 8), (cu[-1], 2, 8), (cu[-1], 4, 8)]))
+    got = oracle.sdpa_backward_varlen(q, k, v, do, cu, causal=True, window=2)
+    for b in (0, 2):
+        a, e = cu[b], cu[b + 1]
+        want = oracle.sdpa_backward(q[a:e], k[a:e], v[a:e], do[a:e], causal=True, window=2)
+        for g, w in zip(got, want):
+            assert np.abs(g[a:e] - w).max() <= TOL
+
+
+def test_backward_sampled_equals_full():
+    """The row / column evaluation used at full size agrees with the whole
+    matrices (small chunk, so several chunks and a ragged last one)."""
+    n, hq, hkv, d = 37, 6, 2, 8
+    q, k, v, do = (_rand(s, 320 + i) for i, s in enumerate(
+        [(n, hq, d), (n, hkv, d), (n, hkv, d), (n, hq, d)]))
+    for causal, window in ((True, 0), (True, 6), (False, 0)):
+        dq, dk, dv = oracle.sdpa_backward(q, k, v, do, causal=causal, window=window)
+        rows = [0, 5, 36]
+        for g in range(hkv):
+            sq, sk, sv = oracle.sdpa_backward_sampled(q, k, v, do, g, rows, rows, causal=causal,
+                                                      window=window, chunk=10)
+            heads = [h for h in range(hq) if h // (hq // hkv) == g]
+            assert np.abs(sq - dq[rows][:, heads]).max() <= TOL
+            assert np.abs(sk - dk[rows, g]).max() <= TOL
+            assert np.abs(sv - dv[rows, g]).max() <= TOL
+
+
+def test_backward_column_sums():
+    """Identities of the gradients at any size: every row of P sums to 1, so
+    the dV rows of a head sum to the dO rows; every row of dS sums to 0, so
+    the dK rows sum to 0 (per query head, hence per KV head)."""
+    n, hq, hkv, d = 23, 4, 2, 8
+    q, k, v, do = (_rand(s, 330 + i) for i, s in enumerate(
+        [(n, hq, d), (n, hkv, d), (n, hkv, d), (n, hq, d)]))
+    _, dk, dv = oracle.sdpa_backward(q, k, v, do, causal=True, window=5)
+    for g in range(hkv):
+        heads = [h for h in range(hq) if h // (hq // hkv) == g]
+        assert np.abs(dv[:, g].sum(axis=0) - do[:, heads].sum(axis=(0, 1))).max() <= TOL
+        assert np.abs(dk[:, g].sum(axis=0)).max() <= TOL
+
+
 def test_kv_bytes(golden):
     for name, layers, kvh, hd, b, n, want in golden("kv_bytes.txt"):
         got = oracle.kv_cache_bytes(int(layers), int(kvh), int(n), int(hd), int(b))
@@ -529,6 +621,7 @@ def _all_pins(golden):
         "align": pin_bottom_right_alignment(),
         "cache": pin_cached_decode_equals_full(),
         "chunked": pin_chunked_prefill_equals_full(),
+        "backward": pin_backward_vs_autograd(),
     }
 
 
