@@ -19,7 +19,7 @@ struct BackwardArgs {
   void* dq;          // [T, Hq, d]
   void* dk;          // [T, Hkv, d]
   void* dv;          // [T, Hkv, d]
-  float* dq_acc;     // workspace [Hq, d/4, T, 4] fp32, zeroed before the main kernel
+  float* dq_acc;     // workspace [T, Hq, d] fp32, zeroed before the main kernel
   float* dvec;       // workspace [Hq, T]: D_i = sum_c dO_ic O_ic
   const int32_t* cu_seqlens;  // nullptr => fixed length N
   int32_t* err;
@@ -32,10 +32,13 @@ struct BackwardArgs {
 // Bytes of workspace the backward pass needs for T packed tokens.
 size_t backward_workspace_bytes(long long T, int Hq, int d);
 
-// D = rowsum(dO * O), dQ accumulation (tensor cores), dQ conversion. The four
-// maps are 64-element x 128-row, 128-byte-swizzled boxes over q, k, v, dout.
+// D = rowsum(dO * O), dQ accumulation (tensor cores), dQ conversion. qmap,
+// kmap, vmap, domap: 64-element x 128-row, 128-byte-swizzled bf16 boxes over
+// q, k, v, dout; dqmap: 32-element (fp32) x 1-head x 32-row, 128-byte-swizzled
+// boxes over the fp32 buffer [T, Hq, d] (the reduce-add target).
 cudaError_t launch_prefill_backward_bf16(const BackwardArgs& a, const CUtensorMap& qmap,
                                          const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                         const CUtensorMap& domap, int num_sms, cudaStream_t s);
+                                         const CUtensorMap& domap, const CUtensorMap& dqmap,
+                                         int num_sms, cudaStream_t s);
 
 }  // namespace pa

@@ -72,6 +72,22 @@ bool encode_3d(CUtensorMap* m, const void* ptr, int d, int heads, long long rows
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 tensor map over a token-major [rows, heads, d] buffer: boxes of 32
+// elements (128 bytes) x 1 head x 32 rows, 128-byte swizzled.
+bool encode_3d_f32_rows32(CUtensorMap* m, const void* ptr, int d, int heads, long long rows) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(heads) * d * 4};
+  const cuuint32_t box[3] = {32, 1, 32};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Pool [num_blocks, block_size, heads, d] described with the dimensions in
 // the order (d, token, head, block): one box of 64 elements x block_size
 // tokens x `box_heads` heads lands in shared memory as `box_heads` head tiles
@@ -241,11 +257,12 @@ int pa_attn_prefill_backward(const void* q, const void* k, const void* v, const 
   a.max_seqlen = msl; a.causal = causal ? 1 : 0; a.window = window > 0 ? window : 0;
   a.scale_log2 = scale_log2(scale, d);
   a.scale = static_cast<float>(softmax_scale(scale, d));
-  CUtensorMap qm, km, vm, dom;
+  CUtensorMap qm, km, vm, dom, dqm;
   if (!encode_3d(&qm, q, d, Hq, T, 128) || !encode_3d(&km, k, d, Hkv, T, 128) ||
-      !encode_3d(&vm, v, d, Hkv, T, 128) || !encode_3d(&dom, dout, d, Hq, T, 128))
+      !encode_3d(&vm, v, d, Hkv, T, 128) || !encode_3d(&dom, dout, d, Hq, T, 128) ||
+      !encode_3d_f32_rows32(&dqm, a.dq_acc, d, Hq, T))
     return PA_ERR_CUDA;
-  const cudaError_t e = pa::launch_prefill_backward_bf16(a, qm, km, vm, dom, sm_count(),
+  const cudaError_t e = pa::launch_prefill_backward_bf16(a, qm, km, vm, dom, dqm, sm_count(),
                                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -25,22 +25,28 @@
 //        dK  += dS^T Q           A = dS^T from shared memory      (SS)
 //        dQ   = dS K             M=128 queries, A = dS^T read MN-major
 //     Everything is kept transposed (keys on TMEM lanes) so dV and dK
-//     accumulate in place. dQ of the tile is added into an fp32 buffer with
-//     vector reductions in L2.
-//      * warp 12 (TMA producer): K, V once per unit; Q, dO and the rows'
-//        lse / D through two stages.
-//      * warp 13 (tcgen05 issuer), in the order S, dP, dV (two halves, as the
-//        halves of P are handed over), dK, dQ, then S of the next tile.
-//      * warps 0-7 (one key row per thread, warps 0-3 / 4-7 take query
-//        columns 0-63 / 64-127): P = 2^(S*scale*log2 e - lse*log2 e) written
-//        as bf16 into the S columns it came from (the A operand of dV), then
-//        dS = P (dP - D) written as bf16 into a 128-byte-swizzled dS^T tile
-//        in shared memory, the operand layout of both the dK and the dQ MMA.
-//      * warps 8-11: read dQ from TMEM and reduce it into the fp32 buffer;
-//        at the end of a unit, write dK (times scale) and dV as bf16.
+//     accumulate in place; dQ of the tile is added into an fp32 buffer
+//     [T, Hq, d] by bulk tensor reduce-adds (performed in L2).
+//      * warp 8 (TMA producer): K, V once per unit; Q, dO and the rows'
+//        -lse*log2(e) and -D through two stages.
+//      * warp 9 (tcgen05 issuer): per tile dV (two halves, as the halves of
+//        P arrive), dP (once the previous tile's dQ has left the TMEM
+//        columns it reuses), S of the next tile (when its Q has landed),
+//        then dK and dQ once dS is in shared memory.
+//      * warps 0-7 (warp (wq, ch): key rows 32*wq.. = its TMEM lane quarter,
+//        query columns 64*ch..), per tile s:
+//          P(s) = 2^(S*scale*log2 e - lse*log2 e), written as bf16 into the S
+//            columns it came from (the A operand of dV);
+//          the read-out of dQ(s-1): TMEM -> registers (freeing the columns
+//            dP(s) needs) -> this warp's rows of the dS^T tile, 128-byte
+//            swizzled -> bulk tensor reduce-add;
+//          dS(s) = P (dP - D), written as bf16 into the 128-byte-swizzled dS^T
+//            tile, the operand layout of both the dK and the dQ MMA, once the
+//            copies of the staged dQ have read it.
+//        At the end of a unit they write dK (times scale) and dV as bf16.
 //     TMEM (512 columns): S^T / P at 0, dP^T at 128 (dQ reuses these columns
 //     once dS has been formed), dV at 256, dK at 256 + d.
-//  3. dQ = scale * buffer, converted to bf16 in [T, Hq, d] layout.
+//  3. dQ = scale * buffer, converted to bf16.
 // All waits are bounded; a wait that gives up raises PA_DEV_TIMEOUT and every
 // role winds down, waiting for its copies and MMAs in flight before TMEM is
 // freed.
@@ -61,10 +67,9 @@ constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile (TMEM lanes of S^T, dP^T, dV, dK)
 constexpr float kLog2e = 1.4426950408889634074f;
 
-constexpr int kDqWarp0 = 8;  // warps 8-11
-constexpr int kLoadWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kThreads = 448;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;  // 8 softmax / gradient warps, producer, MMA issuer
 
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for copies / MMAs already in flight
 
@@ -78,7 +83,7 @@ struct BwCfg {
   static constexpr int OFF_V = TB;
   static constexpr int OFF_DS = 2 * TB;
   static constexpr int OFF_ST = 2 * TB + DSB;            // stage s: Q, then dO
-  static constexpr int OFF_ROW = OFF_ST + NST * 2 * TB;  // stage s: lse*log2(e) [128], D [128]
+  static constexpr int OFF_ROW = OFF_ST + NST * 2 * TB;  // stage s: -lse*log2(e) [128], -D [128]
   static constexpr int OFF_BAR = OFF_ROW + NST * 2 * BM * 4;
   static constexpr int B_KVFULL = 0;
   static constexpr int B_KVFREE = 1;
@@ -177,18 +182,37 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// Expect `bytes` more transaction bytes on an mbarrier without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// dst[tensor box at (x, y, z)] += smem tile (fp32 add, performed in L2).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* m, uint32_t src, int x, int y,
+                                                  int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], "
+      "[%1];" ::"l"(m), "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
                                              uint32_t w) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
                "r"(w)
-               : "memory");
-}
-
-// Four fp32 additions at a 16-byte-aligned global address, performed in L2.
-__device__ __forceinline__ void red_add_v4(float* p, uint32_t x, uint32_t y, uint32_t z,
-                                           uint32_t w) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(x)),
-               "f"(__uint_as_float(y)), "f"(__uint_as_float(z)), "f"(__uint_as_float(w))
                : "memory");
 }
 
@@ -231,7 +255,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap vmap,
-                const __grid_constant__ CUtensorMap domap, const BackwardArgs a) {
+                const __grid_constant__ CUtensorMap domap,
+                const __grid_constant__ CUtensorMap dqmap, const BackwardArgs a) {
   using C = BwCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -266,9 +291,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
       mbar_init(bar(C::B_PRDY + 1), 128);
       mbar_init(bar(C::B_DSRDY), 256);
       mbar_init(bar(C::B_DQFULL), 1);
-      mbar_init(bar(C::B_DQFREE), 128);
+      mbar_init(bar(C::B_DQFREE), 256);
       mbar_init(bar(C::B_ACCFULL), 1);
-      mbar_init(bar(C::B_ACCFREE), 128);
+      mbar_init(bar(C::B_ACCFREE), 256);
       mbar_init(bar(C::B_DRAIN), 1);
       *abort_flag = 0;
       fence_mbar_init();
@@ -312,33 +337,45 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
       ++uc;
       for (int s = 0; s < w.n_steps; ++s, ++gstep) {
         const int st = gstep % C::NST, use = gstep / C::NST;
+        const int g = s / w.n_mt, q0 = (w.mt0 + s % w.n_mt) * BM;
+        const int h = w.kvh * Gq + g;
+        // the rows' statistics, negated (the softmax warps only add them);
+        // fetched before the wait below so that their latency overlaps it
+        float l2[BM / 32], dd[BM / 32];
+#pragma unroll
+        for (int t = 0; t < BM / 32; ++t) {
+          const int i = lane + 32 * t;
+          l2[t] = 0.f;
+          dd[t] = 0.f;
+          if (q0 + i < w.len) {
+            const int64_t ix = static_cast<int64_t>(h) * a.T + w.start + q0 + i;
+            l2[t] = -__ldg(a.lse + ix) * kLog2e;
+            dd[t] = -a.dvec[ix];
+          }
+        }
         // stage free: its MMAs finished, and with them (they waited for dS)
         // the softmax warps' reads of its row statistics
         if (use > 0 && !(ok = wwait(bar(C::B_STFREE + st), (use - 1) & 1, abort_flag))) break;
-        const int g = s / w.n_mt, q0 = (w.mt0 + s % w.n_mt) * BM;
-        const int h = w.kvh * Gq + g;
-        float* rl = rows + st * 2 * BM;
-        for (int i = lane; i < BM; i += 32) {
-          float l2 = 0.f, dd = 0.f;
-          if (q0 + i < w.len) {
-            const int64_t ix = static_cast<int64_t>(h) * a.T + w.start + q0 + i;
-            l2 = __ldg(a.lse + ix) * kLog2e;
-            dd = a.dvec[ix];
-          }
-          rl[i] = l2;
-          rl[BM + i] = dd;
-        }
-        __syncwarp();  // the lanes' stores are ordered before the leader's arrive
+        const uint32_t fb = bar(C::B_STFULL + st);
         if (leader) {
-          const uint32_t fb = bar(C::B_STFULL + st);
+          // the copies go out first; the barrier completes once they have
+          // landed and the leader has arrived after the row statistics
           const uint32_t sq = sST + st * 2 * C::TB;
-          mbar_arrive_expect_tx(fb, 2 * C::TB);
+          mbar_expect_tx(fb, 2 * C::TB);
 #pragma unroll
           for (int p = 0; p < D / 64; ++p) {
             tma_load_3d(sq + p * C::PANEL, &qmap, fb, p * 64, h, w.start + q0);
             tma_load_3d(sq + C::TB + p * C::PANEL, &domap, fb, p * 64, h, w.start + q0);
           }
         }
+        float* rl = rows + st * 2 * BM;
+#pragma unroll
+        for (int t = 0; t < BM / 32; ++t) {
+          rl[lane + 32 * t] = l2[t];
+          rl[BM + lane + 32 * t] = dd[t];
+        }
+        __syncwarp();  // the lanes' stores are ordered before the leader's arrive
+        if (leader) mbar_arrive(fb);
         __syncwarp();
       }
     }
@@ -355,6 +392,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     // Lane 0 issues and commits; the whole warp takes part in every wait.
+    // Order within a tile: dV (as the halves of P arrive), dP (once the
+    // previous tile's dQ has left the columns it reuses), S of the next tile
+    // (if its Q has landed), then dK and dQ once dS is in shared memory.
     constexpr uint32_t idesc_s = umma_idesc_bf16_f32(BN, BM, 0, 0);  // S^T, dP^T
     constexpr uint32_t idesc_kv = umma_idesc_bf16_f32(BN, D, 0, 1);  // dV, dK (B: dO, Q MN-major)
     constexpr uint32_t idesc_q = umma_idesc_bf16_f32(BM, D, 1, 1);   // dQ (A: dS, B: K MN-major)
@@ -369,42 +409,39 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     auto kmaj = [](int kk) -> uint64_t { return 2u * (kk & 3) + 1024u * (kk >> 2); };
     auto mnmaj = [](int kk) -> uint64_t { return 128u * kk; };
     const bool issuer = lane == 0;
+    // S^T = K Q^T of step g (stage g % NST) into the S columns. Those held P
+    // of the previous tile, read by its dV MMAs, which this thread issued
+    // earlier (the tensor core runs one thread's MMAs in issue order).
+    auto issue_s = [&](int g) -> bool {
+      const int st = g % C::NST;
+      if (!wwait(bar(C::B_STFULL + st), (g / C::NST) & 1, abort_flag)) return false;
+      tc_fence_after();
+      const uint64_t q_kmaj = umma_smem_desc_sw128(sST + st * 2 * C::TB, 16, 1024);
+      if (issuer) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + C::TM_S, k_kmaj + kmaj(kk), q_kmaj + kmaj(kk), idesc_s, kk > 0);
+        umma_commit(bar(C::B_SFULL));
+      }
+      __syncwarp();
+      return true;
+    };
     int gstep = 0, uc = 0;
     bool ok = true;
+    bool s_early = false;  // S of the current step already issued
     for (int kr = 0; ok && kr * G < n_units; ++kr) {
       const int u = unit_of(kr, cta, G);
       BUnit w;
       if (u >= n_units || !decode_bunit(a, u, w)) continue;
       if (!(ok = wwait(bar(C::B_KVFULL), uc & 1, abort_flag))) break;
       for (int s = 0; s < w.n_steps; ++s, ++gstep) {
-        const int st = gstep % C::NST, use = gstep / C::NST;
+        const int st = gstep % C::NST;
         const uint32_t sq = sST + st * 2 * C::TB, sdo = sq + C::TB;
         const bool first = s == 0;
-        if (!(ok = wwait(bar(C::B_STFULL + st), use & 1, abort_flag))) break;
-        tc_fence_after();
-        const uint64_t q_kmaj = umma_smem_desc_sw128(sq, 16, 1024);
+        if (!s_early && !(ok = issue_s(gstep))) break;
         const uint64_t do_kmaj = umma_smem_desc_sw128(sdo, 16, 1024);
         const uint64_t q_mn = umma_smem_desc_sw128(sq, C::PANEL, 1024);
         const uint64_t do_mn = umma_smem_desc_sw128(sdo, C::PANEL, 1024);
-        // S^T = K Q^T. Its columns held P of the previous tile, read by that
-        // tile's dV MMAs, which this thread issued earlier (in-order execution).
-        if (issuer) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + C::TM_S, k_kmaj + kmaj(kk), q_kmaj + kmaj(kk), idesc_s, kk > 0);
-          umma_commit(bar(C::B_SFULL));
-        }
-        __syncwarp();
-        // dP^T = V dO^T, into the columns of the previous tile's dQ once read
-        if (gstep > 0 && !(ok = wwait(bar(C::B_DQFREE), (gstep - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        if (issuer) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + C::TM_DP, v_kmaj + kmaj(kk), do_kmaj + kmaj(kk), idesc_s, kk > 0);
-          umma_commit(bar(C::B_DPFULL));
-        }
-        __syncwarp();
         // dV += P^T dO: the previous unit's dK / dV must have been read out
         if (first && uc > 0 && !(ok = wwait(bar(C::B_ACCFREE), (uc - 1) & 1, abort_flag))) break;
         if (!(ok = wwait(bar(C::B_PRDY + 0), gstep & 1, abort_flag))) break;
@@ -425,6 +462,28 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     idesc_kv, 1u);
         }
         __syncwarp();
+        // dP^T = V dO^T, into the columns of the previous tile's dQ once read
+        if (gstep > 0 && !(ok = wwait(bar(C::B_DQFREE), (gstep - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        if (issuer) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + C::TM_DP, v_kmaj + kmaj(kk), do_kmaj + kmaj(kk), idesc_s, kk > 0);
+          umma_commit(bar(C::B_DPFULL));
+        }
+        __syncwarp();
+        // S of the next tile (same unit: same K) if its Q has landed; it
+        // runs while the softmax warps form this tile's dS
+        s_early = false;
+        if (s + 1 < w.n_steps) {
+          const int g1 = gstep + 1;
+          const bool ready = __all_sync(
+              0xFFFFFFFFu, mbar_try_wait(bar(C::B_STFULL + g1 % C::NST), (g1 / C::NST) & 1));
+          if (ready) {
+            if (!(ok = issue_s(g1))) break;
+            s_early = true;
+          }
+        }
         // dK += dS^T Q and dQ = dS K, both reading the dS^T tile
         if (!(ok = wwait(bar(C::B_DSRDY), gstep & 1, abort_flag))) break;
         tc_fence_after();
@@ -453,154 +512,138 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     __syncwarp();
     mbar_wait(bar(C::B_DRAIN), 0, kDrainLimitNs);
     if (!ok && issuer) raise_err(a.err, kDevErrTimeout);
-  } else if (warp >= kDqWarp0) {
-    // ------------------------------------------- dQ read-out, dK / dV epilogue
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // query row (dQ) or key row (dK, dV) of the tile
+  } else {
+    // --------------------------------- P, dS, dQ read-out, dK / dV (warps 0-7)
+    // Warp (wq, ch): key rows 32*wq.. (its TMEM lane quarter) and query
+    // columns 64*ch.. of S^T / dP^T; the same lanes and d columns (d/2)*ch..
+    // of dQ, dK and dV. Per tile s the order is
+    //   P(s), read-out of dQ(s-1), dS(s),
+    // so P(s) runs while the tensor core computes dK / dQ of the previous
+    // tile, and the read-out frees the columns dP(s) needs right after.
+    const int wq = warp & 3, ch = warp >> 2;
+    const int r = wq * 32 + lane;  // key row of the tile; query row of dQ
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tQ = tmem + lane_off + C::TM_DP;
-    const uint32_t tDV = tmem + lane_off + C::TM_DV, tDK = tmem + lane_off + C::TM_DK;
+    const uint32_t tS = tmem + lane_off + C::TM_S + 64 * ch;  // S^T columns of this half
+    const uint32_t tDP = tmem + lane_off + C::TM_DP + 64 * ch;
+    const uint32_t tDQ = tmem + lane_off + C::TM_DP + (D / 2) * ch;  // d columns (d/2)*ch..
+    // this warp's rows of the dS^T tile (32 rows x 128 bytes of panel ch);
+    // between the dQ MMA and the next dS they stage this warp's dQ columns
+    const uint32_t my_ds = sDS + ch * C::PANEL + wq * 32 * 128;
+    const uint32_t ds_row = my_ds + lane * 128;
+    const uint32_t swz = static_cast<uint32_t>(lane & 7);  // = row & 7
+    const uint64_t sl2x2 = f2(a.scale_log2, a.scale_log2);
+
+    // dQ of step gs (query head h, first row q0 of a sequence starting at
+    // `start`, `len` rows): TMEM -> registers (the columns are then free)
+    // -> 128-byte-swizzled staging in this warp's dS^T rows -> bulk tensor
+    // reduce-add into the fp32 buffer [T, Hq, d], performed in L2. Rows past
+    // the sequence hold dQ = 0 exactly (their P and dS are 0), so whole
+    // boxes are added; boxes wholly past it are skipped.
+    auto readout = [&](int gs, int h, int q0, int start, int len) -> bool {
+      if (!wwait(bar(C::B_DQFULL), gs & 1, abort_flag)) return false;
+      tc_fence_after();
+      uint32_t x[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tmem_ld32(tDQ + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[32 * c]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DQFREE));
+      const bool any_live = q0 + wq * 32 < len;
+      const int row0 = start + q0 + wq * 32;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        if (c > 0) {
+          if (lane == 0) bulk_wait_read<0>();  // the previous chunk's copy has read the staging
+          __syncwarp();
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+          st_shared_v4(ds_row + ((static_cast<uint32_t>(m) ^ swz) << 4), x[32 * c + 4 * m],
+                       x[32 * c + 4 * m + 1], x[32 * c + 4 * m + 2], x[32 * c + 4 * m + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && any_live) {
+          tma_reduce_add_3d(&dqmap, my_ds, (D / 2) * ch + 32 * c, h, row0);
+          bulk_commit();
+        }
+      }
+      return true;
+    };
+
     int gstep = 0, uc = 0;
     bool ok = true;
     for (int kr = 0; ok && kr * G < n_units; ++kr) {
       const int u = unit_of(kr, cta, G);
       BUnit w;
       if (u >= n_units || !decode_bunit(a, u, w)) continue;
-      for (int s = 0; s < w.n_steps; ++s, ++gstep) {
-        const int g = s / w.n_mt, q0 = (w.mt0 + s % w.n_mt) * BM;
-        const int h = w.kvh * Gq + g;
-        if (!(ok = wwait(bar(C::B_DQFULL), gstep & 1, abort_flag))) break;
-        tc_fence_after();
-        const bool live = q0 + r < w.len;
-        // buffer layout [Hq][d/4][T][4]: a warp's 32 rows of one column
-        // quad are 512 contiguous bytes
-        float* acc = a.dq_acc + (static_cast<int64_t>(h) * (D / 4) * a.T + w.start + q0 + r) * 4;
-        const int64_t quad = static_cast<int64_t>(a.T) * 4;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t x[64];
-          tmem_ld32(tQ + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-          tmem_ld32(tQ + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-          tmem_wait_ld();
-          if (live) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              red_add_v4(acc + (16 * c + e) * quad, x[4 * e], x[4 * e + 1], x[4 * e + 2],
-                         x[4 * e + 3]);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(bar(C::B_DQFREE));
-        if (s == w.n_steps - 1) {
-          if (!(ok = wwait(bar(C::B_ACCFULL), uc & 1, abort_flag))) break;
-          tc_fence_after();
-          const bool klive = w.k0 + r < w.len;
-          const int64_t row = (static_cast<int64_t>(w.start + w.k0 + r) * a.Hkv + w.kvh) * D;
-          __nv_bfloat16* dvrow = static_cast<__nv_bfloat16*>(a.dv) + row;
-          __nv_bfloat16* dkrow = static_cast<__nv_bfloat16*>(a.dk) + row;
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            const uint32_t t0 = which ? tDK : tDV;
-            __nv_bfloat16* out = which ? dkrow : dvrow;
-            const float sc = which ? a.scale : 1.f;
-            const uint64_t sc2 = f2(sc, sc);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t x[32];
-              tmem_ld32(t0 + 32 * c, x);
-              tmem_wait_ld();
-              if (klive) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                  float lo, hi;
-                  unf2(fmul2(f2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])), sc2),
-                       lo, hi);
-                  pk[e] = pack_bf16(lo, hi);
-                }
-                st_global_v8(out + 32 * c, pk);
-                st_global_v8(out + 32 * c + 16, pk + 8);
-              }
-            }
-          }
-          tc_fence_before();
-          mbar_arrive(bar(C::B_ACCFREE));
-        }
-      }
-      if (!ok) break;
-      ++uc;
-    }
-    if (!ok && lane == 0) raise_err(a.err, kDevErrTimeout);
-  } else {
-    // ------------------------------------------------------ P and dS (warps 0-7)
-    const int wq = warp & 3, ch = warp >> 2;  // TMEM lane quarter, query-column half
-    const int r = wq * 32 + lane;             // key row of the tile
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::TM_S + 64 * ch;  // S^T columns of this half
-    const uint32_t tDP = tmem + lane_off + C::TM_DP + 64 * ch;
-    const uint32_t ds_row = sDS + ch * C::PANEL + r * 128;    // this row of the dS^T panel
-    const uint32_t swz = static_cast<uint32_t>(r & 7);
-    const uint64_t sl2x2 = f2(a.scale_log2, a.scale_log2);
-    int gstep = 0;
-    bool ok = true;
-    for (int kr = 0; ok && kr * G < n_units; ++kr) {
-      const int u = unit_of(kr, cta, G);
-      BUnit w;
-      if (u >= n_units || !decode_bunit(a, u, w)) continue;
       const int j = w.k0 + r;  // key position
+      int prev_h = 0, prev_q0 = 0;
       for (int s = 0; s < w.n_steps; ++s, ++gstep) {
         const int st = gstep % C::NST, use = gstep / C::NST;
-        const int q0 = (w.mt0 + s % w.n_mt) * BM;
+        const int g = s / w.n_mt, q0 = (w.mt0 + s % w.n_mt) * BM;
+        const int h = w.kvh * Gq + g;
         const int qc = q0 + 64 * ch;  // query of this half's first column
         // the stage's row statistics (generic stores released by the
         // producer's arrive) and S^T
         if (!(ok = wwait(bar(C::B_STFULL + st), use & 1, abort_flag))) break;
         if (!(ok = wwait(bar(C::B_SFULL), gstep & 1, abort_flag))) break;
         tc_fence_after();
-        const float* rl = rows + st * 2 * BM + 64 * ch;
-        const float* rd = rl + BM;
+        const float4* nl4 = reinterpret_cast<const float4*>(rows + st * 2 * BM + 64 * ch);
+        const float4* nd4 = nl4 + BM / 4;
         const bool need_mask = (q0 + BM > w.len) || (w.k0 + BN > w.len) ||
                                (a.causal && w.k0 + BN - 1 > q0) ||
                                (a.window > 0 && w.k0 <= q0 + BM - 1 - a.window);
-        float p[64];
+        // P = 2^(S*scale*log2 e - lse*log2 e) for this half's 64 queries,
+        // kept in fp32 (for dS) and stored as bf16 pairs into the first 32 of
+        // the half's S columns (all 64 were read first)
+        uint32_t p[64];
+        tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+        tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t sr[32];
-          tmem_ld32(tS + 32 * cc, sr);
-          tmem_wait_ld();
+        for (int e = 0; e < 16; ++e) {
+          const float4 l = nl4[e];
+          float x0, x1, x2, x3;
+          unf2(ffma2(f2(__uint_as_float(p[4 * e]), __uint_as_float(p[4 * e + 1])), sl2x2,
+                     f2(l.x, l.y)), x0, x1);
+          unf2(ffma2(f2(__uint_as_float(p[4 * e + 2]), __uint_as_float(p[4 * e + 3])), sl2x2,
+                     f2(l.z, l.w)), x2, x3);
+          p[4 * e] = __float_as_uint(ex2(x0));
+          p[4 * e + 1] = __float_as_uint(ex2(x1));
+          p[4 * e + 2] = __float_as_uint(ex2(x2));
+          p[4 * e + 3] = __float_as_uint(ex2(x3));
+        }
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int i = qc + c;
+            const bool vis = i < w.len && j < w.len && (!a.causal || j <= i) &&
+                             (a.window <= 0 || j > i - a.window);
+            if (!vis) p[c] = 0u;
+          }
+        }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
           uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 l2 = *reinterpret_cast<const float2*>(rl + 32 * cc + e);
-            const uint64_t x = ffma2(f2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                     sl2x2, f2(-l2.x, -l2.y));
-            float x0, x1;
-            unf2(x, x0, x1);
-            float p0 = ex2(x0), p1 = ex2(x1);
-            if (need_mask) {
-              const int i0 = qc + 32 * cc + e;
-#pragma unroll
-              for (int t = 0; t < 2; ++t) {
-                const int i = i0 + t;
-                const bool vis = i < w.len && j < w.len && (!a.causal || j <= i) &&
-                                 (a.window <= 0 || j > i - a.window);
-                if (!vis) (t ? p1 : p0) = 0.f;
-              }
-            }
-            p[32 * cc + e] = p0;
-            p[32 * cc + e + 1] = p1;
-            pk[e >> 1] = pack_bf16(p0, p1);
-          }
-          // P of these 32 queries over S columns already read
-          tmem_st16(tS + 16 * cc, pk);
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(__uint_as_float(p[32 * hf + 2 * e]),
+                              __uint_as_float(p[32 * hf + 2 * e + 1]));
+          tmem_st16(tS + 16 * hf, pk);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(C::B_PRDY + ch));
-        // dP^T. Its commit follows the previous tile's dQ read-out, which
-        // followed that tile's dK / dQ MMAs: the dS^T tile is free again.
+        // the previous tile's dQ, which frees the columns of this tile's dP
+        if (s > 0 && !(ok = readout(gstep - 1, prev_h, prev_q0, w.start, w.len))) break;
+        // dP^T; this warp's dS^T rows are free once the copies of the dQ
+        // staged there have read them (the dK / dQ MMAs that read the
+        // previous dS finished before that dQ was read out)
         if (!(ok = wwait(bar(C::B_DPFULL), gstep & 1, abort_flag))) break;
         tc_fence_after();
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t dp[32];
@@ -608,13 +651,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
           tmem_wait_ld();
           uint32_t dsk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 dd = *reinterpret_cast<const float2*>(rd + 32 * cc + e);
-            const uint64_t diff =
-                fadd2(f2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), f2(-dd.x, -dd.y));
-            float d0, d1;
-            unf2(fmul2(diff, f2(p[32 * cc + e], p[32 * cc + e + 1])), d0, d1);
-            dsk[e >> 1] = pack_bf16(d0, d1);
+          for (int e = 0; e < 8; ++e) {
+            const float4 nd = nd4[8 * cc + e];
+            const int c = 32 * cc + 4 * e;
+            float d0, d1, d2, d3;
+            unf2(fmul2(fadd2(f2(__uint_as_float(dp[4 * e]), __uint_as_float(dp[4 * e + 1])),
+                             f2(nd.x, nd.y)),
+                       f2(__uint_as_float(p[c]), __uint_as_float(p[c + 1]))), d0, d1);
+            unf2(fmul2(fadd2(f2(__uint_as_float(dp[4 * e + 2]), __uint_as_float(dp[4 * e + 3])),
+                             f2(nd.z, nd.w)),
+                       f2(__uint_as_float(p[c + 2]), __uint_as_float(p[c + 3]))), d2, d3);
+            dsk[2 * e] = pack_bf16(d0, d1);
+            dsk[2 * e + 1] = pack_bf16(d2, d3);
           }
           // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7)
 #pragma unroll
@@ -624,9 +672,49 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         }
         fence_proxy_async_smem();  // generic stores -> tensor-core reads
         mbar_arrive(bar(C::B_DSRDY));
+        prev_h = h;
+        prev_q0 = q0;
       }
+      if (!ok) break;
+      // the unit's last dQ, then its dK (times scale) and dV
+      if (!(ok = readout(gstep - 1, prev_h, prev_q0, w.start, w.len))) break;
+      if (!(ok = wwait(bar(C::B_ACCFULL), uc & 1, abort_flag))) break;
+      tc_fence_after();
+      const bool klive = j < w.len;
+      const int64_t row = (static_cast<int64_t>(w.start + j) * a.Hkv + w.kvh) * D + (D / 2) * ch;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t t0 = tmem + lane_off + (which ? C::TM_DK : C::TM_DV) + (D / 2) * ch;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(which ? a.dk : a.dv) + row;
+        const float sc = which ? a.scale : 1.f;
+        const uint64_t sc2 = f2(sc, sc);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t x[32];
+          tmem_ld32(t0 + 32 * c, x);
+          tmem_wait_ld();
+          if (klive) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float lo, hi;
+              unf2(fmul2(f2(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1])), sc2), lo,
+                   hi);
+              pk[e] = pack_bf16(lo, hi);
+            }
+            st_global_v8(out + 32 * c, pk);
+            st_global_v8(out + 32 * c + 16, pk + 8);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::B_ACCFREE));
+      ++uc;
     }
-    if (!ok && lane == 0) raise_err(a.err, kDevErrTimeout);
+    if (lane == 0) {
+      bulk_wait<0>();  // every reduction issued has completed
+      if (!ok) raise_err(a.err, kDevErrTimeout);
+    }
   }
 
   tc_fence_before();
@@ -638,42 +726,26 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
 }
 
 // ----------------------------------------------------------------- kernel 3
-// dq[t][h][:] = bf16(scale * acc[h][:][t]); a block converts 32 tokens of one
-// head through shared memory so reads and writes are both contiguous.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const BackwardArgs a) {
-  __shared__ __align__(16) float tile[32][D + 4];
-  const int t0 = blockIdx.x * 32, h = blockIdx.y;
-  const float* acc = a.dq_acc + static_cast<int64_t>(h) * (D / 4) * a.T * 4;
-  for (int i = threadIdx.x; i < 32 * (D / 4); i += 256) {
-    const int cq = i >> 5, tt = i & 31;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t0 + tt < a.T)
-      v = *reinterpret_cast<const float4*>(acc + (static_cast<int64_t>(cq) * a.T + t0 + tt) * 4);
-    *reinterpret_cast<float4*>(&tile[tt][4 * cq]) = v;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 32 * (D / 8); i += 256) {
-    const int tt = i / (D / 8), pc = i % (D / 8);
-    if (t0 + tt >= a.T) continue;
-    const float4 lo = *reinterpret_cast<const float4*>(&tile[tt][8 * pc]);
-    const float4 hi = *reinterpret_cast<const float4*>(&tile[tt][8 * pc + 4]);
-    uint4 out;
-    out.x = pack_bf16(lo.x * a.scale, lo.y * a.scale);
-    out.y = pack_bf16(lo.z * a.scale, lo.w * a.scale);
-    out.z = pack_bf16(hi.x * a.scale, hi.y * a.scale);
-    out.w = pack_bf16(hi.z * a.scale, hi.w * a.scale);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) +
-                              (static_cast<int64_t>(t0 + tt) * a.Hq + h) * D + 8 * pc) = out;
-  }
+// dq = bf16(scale * acc), both [T, Hq, d]; 8 elements per thread.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const BackwardArgs a, int64_t n8) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= n8) return;
+  const float4 lo = reinterpret_cast<const float4*>(a.dq_acc)[2 * i];
+  const float4 hi = reinterpret_cast<const float4*>(a.dq_acc)[2 * i + 1];
+  uint4 out;
+  out.x = pack_bf16(lo.x * a.scale, lo.y * a.scale);
+  out.y = pack_bf16(lo.z * a.scale, lo.w * a.scale);
+  out.z = pack_bf16(hi.x * a.scale, hi.y * a.scale);
+  out.w = pack_bf16(hi.z * a.scale, hi.w * a.scale);
+  reinterpret_cast<uint4*>(a.dq)[i] = out;
 }
 
 int g_bw_attr[2][64];
 
 template <int D>
 cudaError_t launch_all(const BackwardArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                       const CUtensorMap& vmap, const CUtensorMap& domap, int num_sms,
-                       cudaStream_t s) {
+                       const CUtensorMap& vmap, const CUtensorMap& domap,
+                       const CUtensorMap& dqmap, int num_sms, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
@@ -688,9 +760,9 @@ cudaError_t launch_all(const BackwardArgs& a, const CUtensorMap& qmap, const CUt
   const long long warps = static_cast<long long>(a.T) * a.Hq;
   bwd_rowdot_kernel<D><<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(a);
   const unsigned grid = static_cast<unsigned>(a.n_units < num_sms ? a.n_units : num_sms);
-  attn_bwd_kernel<D><<<grid, kThreads, BwCfg<D>::SMEM, s>>>(qmap, kmap, vmap, domap, a);
-  const dim3 cgrid(static_cast<unsigned>((a.T + 31) / 32), static_cast<unsigned>(a.Hq));
-  bwd_dq_convert_kernel<D><<<cgrid, 256, 0, s>>>(a);
+  attn_bwd_kernel<D><<<grid, kThreads, BwCfg<D>::SMEM, s>>>(qmap, kmap, vmap, domap, dqmap, a);
+  const int64_t n8 = static_cast<int64_t>(a.T) * a.Hq * D / 8;
+  bwd_dq_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, s>>>(a, n8);
   return cudaGetLastError();
 }
 
@@ -704,16 +776,17 @@ size_t backward_workspace_bytes(long long T, int Hq, int d) {
 
 cudaError_t launch_prefill_backward_bf16(const BackwardArgs& a0, const CUtensorMap& qmap,
                                          const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                         const CUtensorMap& domap, int num_sms, cudaStream_t s) {
+                                         const CUtensorMap& domap, const CUtensorMap& dqmap,
+                                         int num_sms, cudaStream_t s) {
   BackwardArgs a = a0;
   const long long n_kt = (a.max_seqlen + BN - 1) / BN;
   const long long units = n_kt * a.Hkv * a.B;
   if (units == 0) return cudaSuccess;
-  if (units > INT_MAX || static_cast<long long>(a.T) * a.Hq / 8 + 1 > INT_MAX)
+  if (units > INT_MAX || static_cast<long long>(a.T) * a.Hq * a.d / 8 / 256 + 1 > INT_MAX)
     return cudaErrorInvalidConfiguration;
   a.n_units = static_cast<int>(units);
-  return a.d == 128 ? launch_all<128>(a, qmap, kmap, vmap, domap, num_sms, s)
-                    : launch_all<64>(a, qmap, kmap, vmap, domap, num_sms, s);
+  return a.d == 128 ? launch_all<128>(a, qmap, kmap, vmap, domap, dqmap, num_sms, s)
+                    : launch_all<64>(a, qmap, kmap, vmap, domap, dqmap, num_sms, s);
 }
 
 }  // namespace pa
