@@ -14,6 +14,8 @@ Sources (web pages; cited by title and section):
   KV-cache size formula.
 * "Ли Хунъи, «Машинное обучение» 2026: FlashAttention, KV-кэш и позиционные
   эмбеддинги" (lecture notes) -- the block recurrence and its worked example.
+* "Module 09: Efficient Attention", section "Multi-head Latent Attention: A
+  Different Lever" -- the latent cache, reconstruction and absorption (MLA).
 * "Cache KV, atención flash y optimización de la inferencia" (AI Engineering
   from Scratch, phase 07 lesson 12) -- standard vs tiled attention, the running
   (max, sum) softmax.
@@ -41,7 +43,14 @@ from .paged import (
     decode_paged,
     prefill_paged,
 )
-from .kv_bytes import kv_cache_bytes, kv_bytes_per_token_per_layer
+from .kv_bytes import kv_cache_bytes, kv_bytes_per_token_per_layer, mla_cache_bytes
+from .mla import (
+    mla_absorb_query,
+    mla_up_project,
+    mla_append_paged,
+    mla_decode_latent,
+    mla_decode_explicit,
+)
 
 __all__ = [
     "attention_mask",
@@ -61,4 +70,10 @@ __all__ = [
     "prefill_paged",
     "kv_cache_bytes",
     "kv_bytes_per_token_per_layer",
+    "mla_cache_bytes",
+    "mla_absorb_query",
+    "mla_up_project",
+    "mla_append_paged",
+    "mla_decode_latent",
+    "mla_decode_explicit",
 ]
