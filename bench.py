@@ -57,7 +57,8 @@ def parse():
     ap.add_argument("--workload", default="mixed_window4096",
                     choices=["mixed_window4096", "gqa_decode_llama3_70b", "mha_decode_gpt2",
                              "gqa_prefill_llama3_8b", "chunked_prefill_llama3_8b",
-                             "cow_copy_blocks_llama3_8b", "gqa_prefill_backward_llama3_8b"],
+                             "cow_copy_blocks_llama3_8b", "gqa_prefill_backward_llama3_8b",
+                             "mla_decode_deepseek_v2"],
                     help="other workloads time a single kernel family (profiling aid)")
     ap.add_argument("--only", choices=["prefill", "append", "decode"], default=None,
                     help="run only one phase of the mixed step (profiling aid)")
@@ -93,6 +94,7 @@ KERNEL_SOURCES = {
     "kv_append": ("append_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
     "copy_blocks": ("copy_blocks.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
     "prefill_backward": ("prefill_bwd.cu", "bwd_kernels.h", "pa_ptx.cuh", "capi.cu"),
+    "mla_decode": ("mla_decode.cu", "mla_kernels.h", "pa_ptx.cuh", "capi.cu"),
 }
 
 
@@ -330,6 +332,19 @@ class SingleStep:
             self.phase = "backward"
             # row dot products, main kernel, dQ conversion (plus a memset)
             self.launches = {"backward": 3}
+        elif name == "mla_decode_deepseek_v2":
+            w = inputs.mla_decode_deepseek_v2(device)
+            self.w = w
+            B, H = w["q"].shape[0], w["q"].shape[1]
+            self.out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=device)
+            self.lse = torch.empty((H, B), dtype=torch.float32, device=device)
+            need = binding.mla_decode_workspace_bytes(B, H, w["block_table"].shape[1])
+            self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+            self.flops = 0.0
+            # every cached latent row (512 + 64 bf16 numbers) read once
+            self.dbytes = float(sum(w["lengths"])) * 576 * 2
+            self.phase = "mla"
+            self.launches = {"mla": 2 if need > 0 else 1}
         elif name == "gqa_prefill_llama3_8b":
             w = inputs.gqa_prefill_llama3_8b(device)
             self.w = w
@@ -359,6 +374,10 @@ class SingleStep:
         w = self.w
         if self.phase == "copy":
             self.b.copy_blocks(w["k_cache"], w["v_cache"], w["src"], w["dst"], err_flag=self.err)
+        elif self.phase == "mla":
+            self.b.mla_decode_paged(w["q"], w["cache"], w["block_table"], w["seq_lens"],
+                                    scale=w["scale"], out=self.out, lse=self.lse,
+                                    workspace=self.ws, err_flag=self.err)
         elif self.phase == "backward":
             self.b.attn_prefill_backward(w["q"], w["k"], w["v"], self.out, self.dout, self.lse,
                                          causal=True, cu_seqlens=w["cu_seqlens"],
@@ -558,7 +577,7 @@ def run_ours(args):
     phase_ms = {ph: sum(v) / len(v) for ph, v in times.items()}
     step_ms = sum(phase_ms.values())
     if world > 1:
-        names = ("prefill", "append", "decode", "copy", "backward")
+        names = ("prefill", "append", "decode", "copy", "backward", "mla")
         t = torch.tensor([phase_ms.get(p, 0.0) for p in names] + [step_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         phase_ms = {p: float(t[i]) for i, p in enumerate(names) if p in phase_ms}
@@ -574,6 +593,10 @@ def run_ours(args):
         tf = world * st.flops / (phase_ms["backward"] * 1e-3) / 1e12
         phases_out["backward"] = {"ms": phase_ms["backward"], "value": tf, "unit": "TFLOP/s",
                                   "work": st.flops, "launches": st.launches["backward"]}
+    if "mla" in phase_ms:
+        gb = world * st.dbytes / (phase_ms["mla"] * 1e-3) / 1e9
+        phases_out["mla"] = {"ms": phase_ms["mla"], "value": gb, "unit": "GB/s",
+                             "work": st.dbytes, "launches": st.launches["mla"]}
     if "append" in phase_ms:
         gb = world * st.abytes / (phase_ms["append"] * 1e-3) / 1e9
         phases_out["append"] = {"ms": phase_ms["append"], "value": gb, "unit": "GB/s",
@@ -602,7 +625,8 @@ def run_ours(args):
         r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" \
             else "fallback (recipe)"
         kname = {"prefill": "prefill_bf16", "append": "kv_append", "decode": "decode_bf16",
-                 "copy": "copy_blocks", "backward": "prefill_backward"}[ph]
+                 "copy": "copy_blocks", "backward": "prefill_backward",
+                 "mla": "mla_decode"}[ph]
         r["traffic"] = recorded_traffic(kname, args.workload)
         r["kernel_share"] = phase_ms[ph] / step_ms
         roof[ph] = r
@@ -648,6 +672,7 @@ def run_ours(args):
         "metric": METRIC if args.workload == "mixed_window4096" else
         {"prefill": "causal prefill attention TFLOP/s", "decode": "paged decode KV-read GB/s",
          "backward": "causal prefill attention backward TFLOP/s (10*d per visible pair)",
+         "mla": "MLA decode latent-read GB/s",
          "copy": "copy-on-write block copy GB/s (read + written)"}[head],
         "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,

@@ -80,6 +80,14 @@ def load_library():
     lib.pa_attn_prefill_backward.restype = i32
     lib.pa_attn_prefill_backward_workspace_bytes.argtypes = [i32, i32, i32]
     lib.pa_attn_prefill_backward_workspace_bytes.restype = sz
+    lib.pa_mla_decode_paged.argtypes = [vp, vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32,
+                                        i32, f32, i32, vp, sz, i32, vp, vp]
+    lib.pa_mla_decode_paged.restype = i32
+    lib.pa_mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.pa_mla_decode_workspace_bytes.restype = sz
+    lib.pa_mla_append_paged.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
+                                        vp, vp]
+    lib.pa_mla_append_paged.restype = i32
     _LIB = lib
     return lib
 
@@ -233,6 +241,78 @@ def attn_prefill_backward(q, k, v, o, dout, lse, *, causal=True, window=0, scale
         _ptr(err_flag), _stream(stream))
     _check(st, "attn_prefill_backward")
     return dq, dk, dv
+
+
+MLA_DC, MLA_DR = 512, 64
+
+
+def mla_decode_workspace_bytes(B, H, max_blocks_per_seq, num_splits=0):
+    """Workspace bytes mla_decode_paged needs (0: none)."""
+    return int(load_library().pa_mla_decode_workspace_bytes(int(B), int(H), MLA_DC, MLA_DR,
+                                                            int(max_blocks_per_seq), 16,
+                                                            int(num_splits)))
+
+
+def mla_decode_paged(q, cache, block_table, seq_lens, *, scale, num_splits=0, out=None, lse=None,
+                     return_lse=True, workspace=None, err_flag=None, stream=None):
+    """Latent attention decode: q [B, H, 576] (absorbed content query, then
+    rope query), cache [num_blocks, 16, 576] latent rows [c ; kR],
+    block_table int32 [B, max_blocks], seq_lens int32 [B]. Returns
+    (o [B, H, 512] = sum_j p_ij c_j, lse [H, B])."""
+    lib = load_library()
+    _need(q.dtype == torch.bfloat16 and cache.dtype == torch.bfloat16, "MLA decode takes bf16")
+    for name, t in (("q", q), ("cache", cache)):
+        _cuda_contig(name, t, torch.bfloat16)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("seq_lens", seq_lens, torch.int32)
+    _need(q.dim() == 3 and q.shape[2] == MLA_DC + MLA_DR, "q must be [B, H, 576]")
+    _need(cache.dim() == 3 and cache.shape[1] == 16 and cache.shape[2] == MLA_DC + MLA_DR,
+          "cache must be [num_blocks, 16, 576]")
+    B, H = q.shape[0], q.shape[1]
+    _need(block_table.dim() == 2 and block_table.shape[0] == B, "block_table must be [B, max]")
+    _need(seq_lens.shape == (B,), "seq_lens must be [B]")
+    if out is None:
+        out = torch.empty((B, H, MLA_DC), dtype=torch.bfloat16, device=q.device)
+    _cuda_contig("out", out, torch.bfloat16)
+    _need(out.shape == (B, H, MLA_DC), "out must be [B, H, 512]")
+    if lse is None and return_lse:
+        lse = torch.empty((H, B), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _cuda_contig("lse", lse, torch.float32)
+    need = mla_decode_workspace_bytes(B, H, block_table.shape[1], num_splits)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.pa_mla_decode_paged(_ptr(q), _ptr(cache), _ptr(block_table), block_table.shape[1],
+                                 _ptr(seq_lens), _ptr(out), _ptr(lse), B, H, MLA_DC, MLA_DR, 16,
+                                 cache.shape[0], float(scale), int(num_splits), _ptr(workspace),
+                                 0 if workspace is None else workspace.numel(), _DTYPES[q.dtype],
+                                 _ptr(err_flag), _stream(stream))
+    _check(st, "mla_decode_paged")
+    return out, lse
+
+
+def mla_append_paged(rows_new, cache, block_table, seq_lens, *, cu_new=None, err_flag=None,
+                     stream=None):
+    """Write new latent rows [T_new, row] into cache [num_blocks, 16, row] in
+    place (seq_lens: lengths BEFORE the append; cu_new int32 [B+1] or None
+    for one row per sequence)."""
+    lib = load_library()
+    _need(cache.dtype in _DTYPES, "cache must be bfloat16 or float32")
+    _cuda_contig("rows_new", rows_new, cache.dtype)
+    _cuda_contig("cache", cache, cache.dtype)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("seq_lens", seq_lens, torch.int32)
+    _need(rows_new.dim() == 2 and cache.dim() == 3 and rows_new.shape[1] == cache.shape[2],
+          "rows_new must be [T_new, row] and cache [num_blocks, block_size, row]")
+    B = seq_lens.shape[0]
+    if cu_new is not None:
+        _cuda_contig("cu_new", cu_new, torch.int32)
+    st = lib.pa_mla_append_paged(_ptr(rows_new), _ptr(cache), _ptr(block_table),
+                                 block_table.shape[1], _ptr(seq_lens), _ptr(cu_new),
+                                 rows_new.shape[0], B, cache.shape[2], cache.shape[1],
+                                 cache.shape[0], _DTYPES[cache.dtype], _ptr(err_flag),
+                                 _stream(stream))
+    _check(st, "mla_append_paged")
 
 
 def kv_append_paged(k_new, v_new, k_cache, v_cache, block_table, seq_lens, *, cu_new=None,

@@ -7,6 +7,8 @@
 // KV heads is contiguous both in the input ([T_new, Hkv, d]) and in the pool,
 // so each token is one contiguous copy of Hkv*d*elem bytes, moved as 16-byte
 // vectors by one warp. Bit-exact by construction (no arithmetic on values).
+// With no value tensor (v_new == nullptr) it appends the rows of a single
+// pool, such as the latent rows of an MLA cache.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -79,7 +81,7 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
       const int i = i0 + u * 32 + lane;
       if (i < row_vecs) {
         kv[u] = __ldg(k_new + src + i);
-        vv[u] = __ldg(v_new + src + i);
+        if (v_new) vv[u] = __ldg(v_new + src + i);
       }
     }
 #pragma unroll
@@ -87,7 +89,7 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
       const int i = i0 + u * 32 + lane;
       if (i < row_vecs) {
         k_cache[dst + i] = kv[u];
-        v_cache[dst + i] = vv[u];
+        if (v_new) v_cache[dst + i] = vv[u];
       }
     }
   }

@@ -26,6 +26,10 @@ Named workloads (sizes as in the model shapes they imitate):
                           U[512, 4096] (packed, causal) plus 240 decode
                           requests with cached lengths U[1, 16384]; all new
                           tokens are appended to one shared pool.
+* ``mla_decode_deepseek_v2`` MLA decode with DeepSeek-V2's latent sizes
+                          (d_c = 512, d_R = 64, head_dim 128) and its 128
+                          heads split 8 ways (16 heads per GPU): B=64, cached
+                          lengths U[1024, 32768], bf16 latent rows.
 """
 
 import math
@@ -44,6 +48,8 @@ __all__ = [
     "gqa_decode_llama3_70b",
     "mixed_window4096",
     "chunked_prefill_llama3_8b",
+    "make_mla_cache",
+    "mla_decode_deepseek_v2",
     "WORKLOADS",
 ]
 
@@ -58,6 +64,7 @@ WORKLOAD_SEEDS = {
     "mixed_window4096": 1004,
     "chunked_prefill_llama3_8b": 1005,
     "cow_copy_blocks_llama3_8b": 1006,
+    "mla_decode_deepseek_v2": 1007,
 }
 
 
@@ -140,6 +147,51 @@ def make_paged_cache(capacities, filled, hkv, d, dtype, seed, device="cpu",
         "block_table": table.to(device),
         "num_blocks": num_blocks, "block_size": block_size,
     }
+
+
+def make_mla_cache(capacities, filled, seed, device="cpu", row=576, dtype=torch.bfloat16,
+                   block_size=BLOCK_SIZE, poison=True, spare_blocks=0):
+    """An MLA latent pool [num_blocks, block_size, row] (rows [c ; kR], no
+    head axis) shared by several sequences, with scattered block tables;
+    slots past filled[b] (and spare blocks) are NaN when ``poison``."""
+    gen = make_generator(seed, device)
+    cpu_gen = make_generator(seed + 7919, "cpu")
+    nblk = [math.ceil(c / block_size) for c in capacities]
+    num_blocks = max(sum(nblk) + spare_blocks, 1)
+    width = max(max(nblk, default=1), 1)
+    perm = torch.randperm(num_blocks, generator=cpu_gen)
+    table = torch.full((len(capacities), width), -1, dtype=torch.int32)
+    nxt = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[nxt:nxt + n].to(torch.int32)
+        nxt += n
+    cache = randn((num_blocks, block_size, row), dtype, gen, device)
+    if poison:
+        valid = torch.zeros((num_blocks, block_size), dtype=torch.bool)
+        for b, f in enumerate(filled):
+            nfull = f // block_size
+            if nfull:
+                valid[table[b, :nfull].long()] = True
+            if f % block_size:
+                valid[int(table[b, nfull]), :f % block_size] = True
+        cache[(~valid).to(device)] = torch.tensor(float("nan"), dtype=dtype, device=device)
+    return {"cache": cache, "block_table": table.to(device), "num_blocks": num_blocks,
+            "block_size": block_size}
+
+
+def mla_decode_deepseek_v2(device="cpu", batch=64, heads=16, lo=1024, hi=32768, poison=True):
+    """One MLA decode step (see the module docstring). q holds the absorbed
+    content query and the rope query of each head; seq_lens count the new
+    token's own row."""
+    seed = WORKLOAD_SEEDS["mla_decode_deepseek_v2"]
+    lengths = _uniform_ints(lo, hi, batch, make_generator(seed + 2))
+    c = make_mla_cache(lengths, lengths, seed + 1, device, poison=poison)
+    gen = make_generator(seed + 3, device)
+    q = randn((batch, heads, 576), torch.bfloat16, gen, device)
+    return {"q": q, "cache": c["cache"], "block_table": c["block_table"],
+            "seq_lens": torch.tensor(lengths, dtype=torch.int32, device=device),
+            "lengths": lengths, "num_blocks": c["num_blocks"], "heads": heads,
+            "d_c": 512, "d_rope": 64, "scale": 1.0 / math.sqrt(128 + 64)}
 
 
 def gqa_tiny_f32(device="cpu"):
@@ -267,4 +319,5 @@ WORKLOADS = {
     "gqa_decode_llama3_70b": gqa_decode_llama3_70b,
     "mixed_window4096": mixed_window4096,
     "chunked_prefill_llama3_8b": chunked_prefill_llama3_8b,
+    "mla_decode_deepseek_v2": mla_decode_deepseek_v2,
 }

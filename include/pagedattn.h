@@ -192,6 +192,60 @@ PA_API int pa_attn_prefill_backward(const void* q, const void* k, const void* v,
                                     void* stream);
 
 /*
+ * mla_decode_paged -- multi-head latent attention decode: one query per
+ * sequence attends, in every head, to the sequence's cached latent rows.
+ * "Module 09: Efficient Attention", section "Multi-head Latent Attention: A
+ * Different Lever": the cache keeps per token one latent c_j (d_c numbers)
+ * and one shared rope key kR_j (d_R numbers), no head axis; head i's key is
+ * [W^UK_i c_j ; kR_j] and its value W^UV_i c_j; by absorption ("Why RoPE Has
+ * To Be Decoupled") the query attends the latent directly and the weighted
+ * sum is formed in the latent space ("Ли Хунъи ... 2026", KV-compression
+ * lever 2). With the absorbed query q_i = [W^UK_i^T q^C_i ; q^R_i] supplied
+ * by the caller, this computes
+ *   s_ij = scale * q_i . r_j,   o_i = sum_j softmax_j(s)_ij r_j[0:d_c],
+ * where r_j = [c_j ; kR_j] is cached row j; the caller up-projects o_i with
+ * W^UV_i.
+ *
+ *  q      [B, H, d_c + d_rope] bf16: absorbed content query, then rope query
+ *  cache  [num_blocks, block_size, d_c + d_rope] bf16 rows [c_j ; kR_j], read
+ *         only; token t of sequence b at (block_table[b][t / 16], t % 16)
+ *  block_table int32 [B, max_blocks_per_seq]; seq_lens int32 [B] (keys per
+ *         sequence, the new token's own row included)
+ *  o      [B, H, d_c] bf16 output; lse [H, B] float32 (natural log) or NULL
+ *  scale  > 0 (1/sqrt(d_head + d_rope) for the model's head dim), required
+ *  num_splits 0 = automatic; workspace as in attn_decode_paged, sized by
+ *         pa_mla_decode_workspace_bytes (0 = none needed)
+ * Supported: bf16, d_c = 512, d_rope = 64, block_size 16 (PA_ERR_UNSUPPORTED
+ * otherwise); any H >= 1. A block id outside [0, num_blocks) raises
+ * PA_DEV_BAD_BLOCK and its tokens are skipped; a sequence with no key gets
+ * o = 0 and lse = -inf. Alignment: q, cache, o 16-byte aligned; int32 arrays
+ * and lse 4-byte aligned; workspace 256-byte aligned.
+ */
+PA_API size_t pa_mla_decode_workspace_bytes(int B, int H, int d_c, int d_rope,
+                                            int max_blocks_per_seq, int block_size,
+                                            int num_splits);
+
+PA_API int pa_mla_decode_paged(const void* q, const void* cache, const int32_t* block_table,
+                               int max_blocks_per_seq, const int32_t* seq_lens, void* o,
+                               float* lse, int B, int H, int d_c, int d_rope, int block_size,
+                               int num_blocks, float scale, int num_splits, void* workspace,
+                               size_t workspace_bytes, pa_dtype dtype, int32_t* err_flag,
+                               void* stream);
+
+/*
+ * mla_append_paged -- write new tokens' latent rows ([c ; kR], row_elems
+ * numbers each) into an MLA cache [num_blocks, block_size, row_elems]: the
+ * single-pool form of kv_append_paged (same table, seq_lens, cu_new and
+ * error semantics; a byte copy). row_elems * element size must be a
+ * multiple of 16; pointers 16-byte aligned, int32 arrays 4-byte aligned.
+ */
+PA_API int pa_mla_append_paged(const void* rows_new, void* cache, const int32_t* block_table,
+                               int max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* cu_new, int num_new_tokens, int B, int row_elems,
+                               int block_size, int num_blocks, pa_dtype dtype,
+                               int32_t* err_flag, void* stream);
+
+/*
  * kv_append_paged -- write new tokens' keys and values into the paged pools.
  * "Module 09: Efficient Attention", section "Code: A Paged KV Cache from
  * Scratch": token t of a sequence lives at (block_table[t / block_size],

@@ -35,6 +35,7 @@ def test_header_declares_the_entry_points():
     for name in ("pa_attn_prefill", "pa_attn_prefill_paged", "pa_kv_append_paged",
                  "pa_copy_blocks", "pa_attn_decode_paged", "pa_decode_workspace_bytes",
                  "pa_attn_prefill_backward", "pa_attn_prefill_backward_workspace_bytes",
+                 "pa_mla_decode_paged", "pa_mla_decode_workspace_bytes", "pa_mla_append_paged",
                  "pa_status_str"):
         assert name in syms
 
@@ -107,6 +108,45 @@ def test_backward_host_validation(lib):
     need = lib.pa_attn_prefill_backward_workspace_bytes(100, 4, 64)
     assert need == (100 * 4 * 64 * 4 + 255) // 256 * 256 + (100 * 4 * 4 + 255) // 256 * 256
     assert lib.pa_attn_prefill_backward_workspace_bytes(100, 4, 96) == 0
+
+
+def _mla(lib, **kw):
+    a = dict(q=FAKE, c=FAKE, table=FAKE, mb=8, sl=FAKE, o=FAKE, lse=None, B=2, H=16, dc=512,
+             dr=64, bs=16, nb=16, scale=0.1, ns=1, ws=None, wsb=0, dt=0, err=None, stream=None)
+    a.update(kw)
+    return lib.pa_mla_decode_paged(a["q"], a["c"], a["table"], a["mb"], a["sl"], a["o"], a["lse"],
+                                   a["B"], a["H"], a["dc"], a["dr"], a["bs"], a["nb"], a["scale"],
+                                   a["ns"], a["ws"], a["wsb"], a["dt"], a["err"], a["stream"])
+
+
+def test_mla_host_validation(lib):
+    assert _mla(lib, scale=0.0) == PA_ERR_INVALID_ARG          # the scale is required
+    assert _mla(lib, scale=float("nan")) == PA_ERR_INVALID_ARG
+    assert _mla(lib, H=0) == PA_ERR_INVALID_ARG
+    assert _mla(lib, q=None) == PA_ERR_INVALID_ARG
+    assert _mla(lib, c=FAKE + 8) == PA_ERR_INVALID_ARG           # 16-byte alignment
+    assert _mla(lib, dc=256) == PA_ERR_UNSUPPORTED               # latent width 512 only
+    assert _mla(lib, dr=32) == PA_ERR_UNSUPPORTED
+    assert _mla(lib, bs=32) == PA_ERR_UNSUPPORTED
+    assert _mla(lib, dt=1) == PA_ERR_UNSUPPORTED
+    assert _mla(lib, ns=4) == PA_ERR_WORKSPACE                   # split ranges need a workspace
+    assert lib.pa_mla_decode_workspace_bytes(2, 16, 512, 64, 8, 16, 1) == 0
+    n = 2 * 16 * 4
+    assert lib.pa_mla_decode_workspace_bytes(2, 16, 512, 64, 8, 16, 4) == \
+        (n * 512 * 4 + 255) // 256 * 256 + (n * 4 + 255) // 256 * 256
+    assert lib.pa_mla_decode_workspace_bytes(2, 16, 256, 64, 8, 16, 4) == 0
+
+    def app(**kw):
+        a = dict(rows=FAKE, c=FAKE, table=FAKE, mb=4, sl=FAKE, cu=None, tn=2, B=2, row=576, bs=16,
+                 nb=8, dt=0, err=None, stream=None)
+        a.update(kw)
+        return lib.pa_mla_append_paged(a["rows"], a["c"], a["table"], a["mb"], a["sl"], a["cu"],
+                                       a["tn"], a["B"], a["row"], a["bs"], a["nb"], a["dt"],
+                                       a["err"], a["stream"])
+    assert app(tn=3) == PA_ERR_INVALID_ARG                       # one row per sequence without cu
+    assert app(row=100) == PA_ERR_INVALID_ARG                    # rows must be 16-byte multiples
+    assert app(c=FAKE + 4) == PA_ERR_INVALID_ARG
+    assert app(tn=0, cu=FAKE) == PA_OK                           # nothing to append, no launch
 
 
 def _prefill_paged(lib, **kw):
