@@ -89,12 +89,13 @@ def load_peaks():
 
 # Sources whose change invalidates a kernel's recorded DRAM traffic.
 KERNEL_SOURCES = {
-    "prefill_bf16": ("prefill_sm103.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
-    "decode_bf16": ("decode_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
-    "kv_append": ("append_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
-    "copy_blocks": ("copy_blocks.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu"),
-    "prefill_backward": ("prefill_bwd.cu", "bwd_kernels.h", "pa_ptx.cuh", "capi.cu"),
-    "mla_decode": ("mla_decode.cu", "mla_kernels.h", "pa_ptx.cuh", "capi.cu"),
+    "prefill_bf16": ("prefill_sm103.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu", "host_util.h"),
+    "decode_bf16": ("decode_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu", "host_util.h"),
+    "kv_append": ("append_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu", "host_util.h"),
+    "copy_blocks": ("copy_blocks.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu", "host_util.h"),
+    "prefill_backward": ("prefill_bwd.cu", "bwd_kernels.h", "pa_ptx.cuh", "capi_bwd.cu",
+                         "host_util.h"),
+    "mla_decode": ("mla_decode.cu", "mla_kernels.h", "pa_ptx.cuh", "capi_mla.cu", "host_util.h"),
 }
 
 

@@ -470,14 +470,14 @@ MlaPlan plan_mla_decode(int B, int H, int max_blocks, int num_splits_req, int sm
   if (num_splits_req > 0) {
     chunk = (eff + num_splits_req - 1) / num_splits_req;
   } else {
-    // about two waves of CTAs (two CTAs per SM fit for 16 heads, one for 32),
-    // ranges of at least 4 blocks
+    // ranges sized so that, were every sequence as long as the table, the
+    // call would fill the CTA slots (two per SM for 16 heads, one for 32)
+    // about 3.5 times: sequences of mixed lengths then leave about two
+    // waves, short enough a tail; at least 8 blocks per range
     const long long units = static_cast<long long>(B) * p.head_chunks;
     const long long slots = static_cast<long long>(sms) * (p.ng == 1 ? 2 : 1);
-    long long splits = (2 * slots + units - 1) / units;
-    if (splits < 1) splits = 1;
-    long long c = (eff + splits - 1) / splits;
-    if (c < 4) c = 4;
+    long long c = (units * eff * 2 + 7 * slots - 1) / (7 * slots);
+    if (c < 8) c = 8;
     chunk = static_cast<int>(c);
   }
   if (chunk > eff) chunk = eff;
