@@ -216,24 +216,36 @@ def sdpa_backward(q, k, v, dout, *, causal, window=0, scale=None):
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    has_key = allowed.any(axis=1)
     for h in range(hq):
         g = kv_head_of(h, hq, hkv)
-        s = np.where(allowed, scale * (q[:, h, :] @ k[:, g, :].T), -np.inf)
-        p = np.zeros_like(s)
-        if has_key.any():
-            sv = s[has_key]
-            e = np.exp(sv - sv.max(axis=1, keepdims=True))
-            p[has_key] = e / e.sum(axis=1, keepdims=True)
-        o = p @ v[:, g, :]
-        do = dout[:, h, :]
-        dv[:, g, :] += p.T @ do
-        dp = do @ v[:, g, :].T
-        drow = (do * o).sum(axis=1, keepdims=True)
-        ds = p * (dp - drow)
-        dq[:, h, :] = scale * (ds @ k[:, g, :])
-        dk[:, g, :] += scale * (ds.T @ q[:, h, :])
+        dq_h, dk_h, dv_h = _head_backward(q[:, h, :], k[:, g, :], v[:, g, :], dout[:, h, :],
+                                          allowed, scale)
+        dq[:, h, :] = dq_h
+        dk[:, g, :] += dk_h
+        dv[:, g, :] += dv_h
     return dq, dk, dv
+
+
+def _softmax_backward(p, dp, drow):
+    """dS = P * (dP - D): the softmax's Jacobian applied row by row."""
+    return p * (dp - drow)
+
+
+def _head_backward(qh, kg, vg, doh, allowed, scale):
+    """One query head's (dq, dk, dv) contributions; the forward recomputed."""
+    s = np.where(allowed, scale * (qh @ kg.T), -np.inf)
+    p = np.zeros_like(s)
+    has_key = allowed.any(axis=1)
+    if has_key.any():
+        sv = s[has_key]
+        e = np.exp(sv - sv.max(axis=1, keepdims=True))
+        p[has_key] = e / e.sum(axis=1, keepdims=True)
+    o = p @ vg
+    dv = p.T @ doh
+    dp = doh @ vg.T
+    drow = (doh * o).sum(axis=1, keepdims=True)
+    ds = _softmax_backward(p, dp, drow)
+    return scale * (ds @ kg), scale * (ds.T @ qh), dv
 
 
 def sdpa_backward_varlen(q, k, v, dout, cu_seqlens, *, causal, window=0, scale=None):

@@ -665,3 +665,37 @@ def test_planted_mistakes_are_caught(golden, monkeypatch, mistake):
     except Exception:
         return  # a pin raised: caught
     assert any(v > 1e-9 for v in pins.values()), pins
+
+
+@pytest.mark.parametrize("mistake", ["ds_without_d", "ds_wrong_sign", "dk_unscaled",
+                                     "dv_untransposed", "dq_from_v"])
+def test_planted_backward_mistakes_are_caught(mistake, monkeypatch):
+    """Plausible slips in the gradient formulas each fail the autograd pin."""
+    if mistake == "ds_without_d":
+        monkeypatch.setattr(oatt, "_softmax_backward", lambda p, dp, drow: p * dp)
+    elif mistake == "ds_wrong_sign":
+        monkeypatch.setattr(oatt, "_softmax_backward", lambda p, dp, drow: p * (drow - dp))
+    else:
+        orig = oatt._head_backward
+
+        def head(qh, kg, vg, doh, allowed, scale):
+            dq, dk, dv = orig(qh, kg, vg, doh, allowed, scale)
+            if mistake == "dk_unscaled":
+                return dq, dk / scale, dv
+            if mistake == "dv_untransposed":  # P dO instead of P^T dO (square in the pins)
+                s = np.where(allowed, scale * (qh @ kg.T), -np.inf)
+                p = np.exp(s - s.max(axis=1, keepdims=True))
+                p /= p.sum(axis=1, keepdims=True)
+                return dq, dk, p @ doh
+            # dQ = scale dS V instead of scale dS K
+            return scale * (_ds(qh, kg, vg, doh, allowed, scale) @ vg), dk, dv
+        monkeypatch.setattr(oatt, "_head_backward", head)
+    assert pin_backward_vs_autograd() > 1e-6
+
+
+def _ds(qh, kg, vg, doh, allowed, scale):
+    s = np.where(allowed, scale * (qh @ kg.T), -np.inf)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    o = p @ vg
+    return p * (doh @ vg.T - (doh * o).sum(axis=1, keepdims=True))

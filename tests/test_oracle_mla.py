@@ -134,3 +134,24 @@ def test_mla_append_writes_rows_at_their_slots():
     assert np.array_equal(out[0, 0], rows[2])          # position 4 -> second block
     assert np.array_equal(out[3, 3], rows[3]) and np.array_equal(out[1, 0], rows[4])
     assert np.count_nonzero(out) == np.count_nonzero(rows)
+
+
+def test_planted_mla_mistakes_are_caught(monkeypatch):
+    """Dropping the rope part of the score, or taking the values from the
+    wrong slice of the row, each break the absorption identity."""
+    orig = oracle.mla_decode_latent
+
+    def no_rope(q, pool, tables, lens, *, d_c, scale, block_size=16):
+        q = np.array(q, dtype=float, copy=True)
+        q[..., d_c:] = 0.0
+        return orig(q, pool, tables, lens, d_c=d_c, scale=scale, block_size=block_size)
+
+    def shifted_values(q, pool, tables, lens, *, d_c, scale, block_size=16):
+        o, lse = orig(q, pool, tables, lens, d_c=d_c, scale=scale, block_size=block_size)
+        rolled = np.roll(np.array(pool, dtype=float), -1, axis=-1)
+        o2, _ = orig(q, rolled, tables, lens, d_c=d_c, scale=scale, block_size=block_size)
+        return o2, lse
+
+    for bad in (no_rope, shifted_values):
+        monkeypatch.setattr(oracle, "mla_decode_latent", bad)
+        assert pin_mla_absorption() > 1e-6
