@@ -29,10 +29,10 @@
 //     [T, Hq, d] by bulk tensor reduce-adds (performed in L2).
 //      * warp 8 (TMA producer): K, V once per unit; Q, dO and the rows'
 //        -lse*log2(e) and -D through two stages.
-//      * warp 9 (tcgen05 issuer): per tile dV (two halves, as the halves of
-//        P arrive), dP (once the previous tile's dQ has left the TMEM
-//        columns it reuses), S of the next tile (when its Q has landed),
-//        then dK and dQ once dS is in shared memory.
+//      * warp 9 (tcgen05 issuer): per tile dP (once the previous tile's dQ
+//        has left the TMEM columns it reuses), dV (two halves, as the halves
+//        of P arrive), S of the next tile (when its Q has landed), then dK
+//        and dQ once dS is in shared memory.
 //      * warps 0-7 (warp (wq, ch): key rows 32*wq.. = its TMEM lane quarter,
 //        query columns 64*ch..), per tile s:
 //          P(s) = 2^(S*scale*log2 e - lse*log2 e), written as bf16 into the S
@@ -392,8 +392,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     // Lane 0 issues and commits; the whole warp takes part in every wait.
-    // Order within a tile: dV (as the halves of P arrive), dP (once the
-    // previous tile's dQ has left the columns it reuses), S of the next tile
+    // Order within a tile: dP (once the previous tile's dQ has left the
+    // columns it reuses), dV (as the halves of P arrive), S of the next tile
     // (if its Q has landed), then dK and dQ once dS is in shared memory.
     constexpr uint32_t idesc_s = umma_idesc_bf16_f32(BN, BM, 0, 0);  // S^T, dP^T
     constexpr uint32_t idesc_kv = umma_idesc_bf16_f32(BN, D, 0, 1);  // dV, dK (B: dO, Q MN-major)
@@ -442,6 +442,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         const uint64_t do_kmaj = umma_smem_desc_sw128(sdo, 16, 1024);
         const uint64_t q_mn = umma_smem_desc_sw128(sq, C::PANEL, 1024);
         const uint64_t do_mn = umma_smem_desc_sw128(sdo, C::PANEL, 1024);
+        // dP^T = V dO^T first (dS waits for it; dV does not), into the
+        // columns of the previous tile's dQ once that has been read out
+        if (gstep > 0 && !(ok = wwait(bar(C::B_DQFREE), (gstep - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        if (issuer) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_ss(tmem + C::TM_DP, v_kmaj + kmaj(kk), do_kmaj + kmaj(kk), idesc_s, kk > 0);
+          umma_commit(bar(C::B_DPFULL));
+        }
+        __syncwarp();
         // dV += P^T dO: the previous unit's dK / dV must have been read out
         if (first && uc > 0 && !(ok = wwait(bar(C::B_ACCFREE), (uc - 1) & 1, abort_flag))) break;
         if (!(ok = wwait(bar(C::B_PRDY + 0), gstep & 1, abort_flag))) break;
@@ -460,16 +471,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
           for (int kk = 4; kk < 8; ++kk)
             umma_ts(tmem + C::TM_DV, tmem + C::TM_S + 64 + 8 * (kk - 4), do_mn + mnmaj(kk),
                     idesc_kv, 1u);
-        }
-        __syncwarp();
-        // dP^T = V dO^T, into the columns of the previous tile's dQ once read
-        if (gstep > 0 && !(ok = wwait(bar(C::B_DQFREE), (gstep - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        if (issuer) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_ss(tmem + C::TM_DP, v_kmaj + kmaj(kk), do_kmaj + kmaj(kk), idesc_s, kk > 0);
-          umma_commit(bar(C::B_DPFULL));
         }
         __syncwarp();
         // S of the next tile (same unit: same K) if its Q has landed; it
