@@ -78,6 +78,26 @@ def dist_info():
     return world, rank, local
 
 
+PHASES = ("prefill", "append", "decode", "copy", "backward", "mla")
+
+
+def max_over_ranks(phase_ms, step_ms, device):
+    """Replicas' phase times reduced to the slowest rank's (element-wise max
+    over the process group; the identity without one)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return dict(phase_ms), step_ms
+    t = torch.tensor([phase_ms.get(p, 0.0) for p in PHASES] + [step_ms], dtype=torch.float64,
+                     device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return {p: float(t[i]) for i, p in enumerate(PHASES) if p in phase_ms}, float(t[len(PHASES)])
+
+
+def whole_job_rate(work_per_rank, world, ms):
+    """All replicas' work over the slowest rank's time, per second."""
+    return world * work_per_rank / (ms * 1e-3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -577,37 +597,32 @@ def run_ours(args):
 
     phase_ms = {ph: sum(v) / len(v) for ph, v in times.items()}
     step_ms = sum(phase_ms.values())
-    if world > 1:
-        names = ("prefill", "append", "decode", "copy", "backward", "mla")
-        t = torch.tensor([phase_ms.get(p, 0.0) for p in names] + [step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        phase_ms = {p: float(t[i]) for i, p in enumerate(names) if p in phase_ms}
-        step_ms = float(t[len(names)])
+    phase_ms, step_ms = max_over_ranks(phase_ms, step_ms, dev)
 
     # throughput per phase (whole job: all replicas' work over the slowest rank)
     phases_out = {}
     if "prefill" in phase_ms:
-        tf = world * st.flops / (phase_ms["prefill"] * 1e-3) / 1e12
+        tf = whole_job_rate(st.flops, world, phase_ms["prefill"]) / 1e12
         phases_out["prefill"] = {"ms": phase_ms["prefill"], "value": tf, "unit": "TFLOP/s",
                                  "work": st.flops, "launches": st.launches["prefill"]}
     if "backward" in phase_ms:
-        tf = world * st.flops / (phase_ms["backward"] * 1e-3) / 1e12
+        tf = whole_job_rate(st.flops, world, phase_ms["backward"]) / 1e12
         phases_out["backward"] = {"ms": phase_ms["backward"], "value": tf, "unit": "TFLOP/s",
                                   "work": st.flops, "launches": st.launches["backward"]}
     if "mla" in phase_ms:
-        gb = world * st.dbytes / (phase_ms["mla"] * 1e-3) / 1e9
+        gb = whole_job_rate(st.dbytes, world, phase_ms["mla"]) / 1e9
         phases_out["mla"] = {"ms": phase_ms["mla"], "value": gb, "unit": "GB/s",
                              "work": st.dbytes, "launches": st.launches["mla"]}
     if "append" in phase_ms:
-        gb = world * st.abytes / (phase_ms["append"] * 1e-3) / 1e9
+        gb = whole_job_rate(st.abytes, world, phase_ms["append"]) / 1e9
         phases_out["append"] = {"ms": phase_ms["append"], "value": gb, "unit": "GB/s",
                                 "work": st.abytes, "launches": st.launches["append"]}
     if "copy" in phase_ms:
-        gb = world * st.cbytes / (phase_ms["copy"] * 1e-3) / 1e9
+        gb = whole_job_rate(st.cbytes, world, phase_ms["copy"]) / 1e9
         phases_out["copy"] = {"ms": phase_ms["copy"], "value": gb, "unit": "GB/s",
                               "work": st.cbytes, "launches": st.launches["copy"]}
     if "decode" in phase_ms:
-        gb = world * st.dbytes / (phase_ms["decode"] * 1e-3) / 1e9
+        gb = whole_job_rate(st.dbytes, world, phase_ms["decode"]) / 1e9
         phases_out["decode"] = {"ms": phase_ms["decode"], "value": gb, "unit": "GB/s",
                                 "work": st.dbytes, "launches": st.launches["decode"]}
 
