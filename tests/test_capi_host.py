@@ -136,6 +136,26 @@ def test_mla_host_validation(lib):
         (n * 512 * 4 + 255) // 256 * 256 + (n * 4 + 255) // 256 * 256
     assert lib.pa_mla_decode_workspace_bytes(2, 16, 256, 64, 8, 16, 4) == 0
 
+
+def _mla_ws(n):
+    return (n * 512 * 4 + 255) // 256 * 256 + (n * 4 + 255) // 256 * 256
+
+
+def test_mla_range_planner(lib):
+    """Automatic ranges (no GPU: 148 SMs assumed): sized so that full-length
+    tables would fill the CTA slots (two per SM for 16 heads, one for 32)
+    about 3.5 times, at least 8 blocks per range, one range for short
+    tables."""
+    # 64 sequences x 16 heads, 2048-block tables: ranges of 127 blocks -> 17
+    assert lib.pa_mla_decode_workspace_bytes(64, 16, 512, 64, 2048, 16, 0) == _mla_ws(64 * 16 * 17)
+    # 128 heads (four chunks of 32, one CTA per SM): ranges of 1013 blocks -> 3
+    assert lib.pa_mla_decode_workspace_bytes(64, 128, 512, 64, 2048, 16, 0) == \
+        _mla_ws(64 * 128 * 3)
+    # one short sequence: a single range, no workspace
+    assert lib.pa_mla_decode_workspace_bytes(1, 16, 512, 64, 4, 16, 0) == 0
+    # one long sequence: at least 8 blocks per range
+    assert lib.pa_mla_decode_workspace_bytes(1, 16, 512, 64, 100, 16, 0) == _mla_ws(16 * 13)
+
     def app(**kw):
         a = dict(rows=FAKE, c=FAKE, table=FAKE, mb=4, sl=FAKE, cu=None, tn=2, B=2, row=576, bs=16,
                  nb=8, dt=0, err=None, stream=None)
