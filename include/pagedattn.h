@@ -44,7 +44,14 @@
  *    caller reads the flag after synchronising. The library never clears it.
  *  - dtype PA_BF16: bf16 inputs and outputs, fp32 accumulation. PA_F32: fp32
  *    inputs and outputs (a CUDA-core correctness path), fp32 accumulation.
- *  - Head dimension d must be 64 or 128.
+ *  - Head dimension d must be 64 or 128 (MLA: latent rows of d_c = 512 plus
+ *    d_rope = 64).
+ *
+ * Beyond the forward pass the library has the backward pass of the prefill
+ * (pa_attn_prefill_backward), chunked prefill into a paged cache
+ * (pa_attn_prefill_paged), block copies for copy-on-write (pa_copy_blocks)
+ * and multi-head latent attention decode over a paged latent cache
+ * (pa_mla_decode_paged, pa_mla_append_paged).
  */
 #ifndef PAGEDATTN_H_
 #define PAGEDATTN_H_
