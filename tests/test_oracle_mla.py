@@ -4,6 +4,7 @@ per-head reconstruction, an independent library routine, paging invariance
 and the byte-exact append."""
 
 import numpy as np
+import pytest
 import torch
 import torch.nn.functional as F
 
@@ -155,3 +156,26 @@ def test_planted_mla_mistakes_are_caught(monkeypatch):
     for bad in (no_rope, shifted_values):
         monkeypatch.setattr(oracle, "mla_decode_latent", bad)
         assert pin_mla_absorption() > 1e-6
+
+
+def test_mla_cache_recipe():
+    """The seeded MLA pool: every sequence's blocks are distinct, written
+    slots are finite, the rest (and spare blocks) are NaN, and the same seed
+    gives the same bits."""
+    from flashattention_paged_kv_fwd_b300 import inputs
+
+    lens = [5, 16, 33]
+    a = inputs.make_mla_cache(lens, lens, 9, "cpu", spare_blocks=2)
+    b = inputs.make_mla_cache(lens, lens, 9, "cpu", spare_blocks=2)
+    assert torch.equal(a["cache"].view(torch.int16), b["cache"].view(torch.int16))
+    table = a["block_table"]
+    used = [int(x) for x in table.flatten() if int(x) >= 0]
+    assert len(used) == len(set(used)) == sum((n + 15) // 16 for n in lens)
+    cache = a["cache"].float()
+    finite = torch.isfinite(cache).all(dim=-1)
+    for bi, n in enumerate(lens):
+        for t in range(n):
+            assert bool(finite[int(table[bi, t // 16]), t % 16])
+    assert int(finite.sum()) == sum(lens)  # every other slot is poisoned
+    w = inputs.mla_decode_deepseek_v2("cpu", batch=3, lo=20, hi=40)
+    assert w["q"].shape == (3, 16, 576) and w["scale"] == pytest.approx(1 / 192 ** 0.5)
