@@ -21,6 +21,13 @@ of another buffer read, so that L2 holds neither inputs nor dirty lines).
 
 ``--impl reference`` times the CPU oracle (fp64, full score rows, naive block
 table walk) on a bounded sample of the same workload instead.
+
+``--workload`` times one kernel family on its own workload and prints the
+same line with that family's metric: ``gqa_prefill_llama3_8b`` and
+``chunked_prefill_llama3_8b`` (TFLOP/s), ``gqa_prefill_backward_llama3_8b``
+(TFLOP/s, 10*d FLOPs per visible pair and query head),
+``gqa_decode_llama3_70b``, ``mha_decode_gpt2`` and ``mla_decode_deepseek_v2``
+(GB/s of cache read), ``cow_copy_blocks_llama3_8b`` (GB/s read + written).
 """
 
 import argparse
