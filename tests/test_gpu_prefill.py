@@ -79,7 +79,7 @@ def test_prefill_bf16_fixed_length_and_empty_sequences():
 
 def test_prefill_large_scores_rescale():
     """Scores that grow along the sequence force the running max to move by
-    more than the lazy-rescale threshold many times."""
+    more than the lazy-rescale threshold (2^8) many times."""
     lengths = [600]
     w = inputs.make_prefill(lengths, 4, 2, 64, torch.bfloat16, 5, "cuda")
     ramp = torch.linspace(0.2, 6.0, 600, device="cuda")[:, None, None]
@@ -89,8 +89,41 @@ def test_prefill_large_scores_rescale():
                                   max_seqlen=600)
     want_o, want_lse = oracle.sdpa_varlen(q.cpu(), k.cpu(), w["v"].cpu(), [0, 600], [0, 600],
                                           causal=True)
+    assert float(np.abs(want_lse).max()) > 40.0  # the running max really moves far
     assert_close_bf16(o, want_o, "o")
-    assert_close(lse.cpu(), want_lse, "lse", 2e-3 * max(1.0, float(np.abs(want_lse).max()) / 10))
+    assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
+
+
+@pytest.mark.parametrize("hq,hkv,window", [(8, 2, 0), (6, 2, 0), (8, 2, 200), (4, 4, 90)])
+def test_prefill_rescale_within_and_across_tiles(hq, hkv, window):
+    """Key magnitudes that climb steeply in short bursts: within one 128-key
+    tile a row's maximum score rises past 2^8 times the running max several
+    times, and it keeps rising across tiles, so the lazy rescale fires both on
+    consecutive tiles and after long stretches without one. (8, 2) pairs two
+    query heads of a KV group per unit, (6, 2) pairs two row tiles of one
+    head, the windowed cases drop the early keys from a row's range while its
+    max is still rising, so its max is reached inside the window."""
+    lengths = [700, 333]
+    d = 128
+    w = inputs.make_prefill(lengths, hq, hkv, d, torch.bfloat16, 40 + hq + window, "cuda")
+    T = sum(lengths)
+    pos = torch.cat([torch.arange(n, device="cuda") for n in lengths]).float()
+    # a staircase of 48-key steps, each ~1.6x the last, on top of a slow ramp
+    ramp = (0.15 * 1.6 ** torch.floor(pos / 48.0) * (1.0 + pos / 700.0)).clamp(max=8.0)
+    k = (w["k"].float() * ramp[:, None, None]).to(torch.bfloat16)
+    q = (w["q"].float() * 2.5).to(torch.bfloat16)
+    cu = w["cu_seqlens"]
+    err = binding.new_err_flag()
+    o, lse = binding.attn_prefill(q, k, w["v"], causal=True, window=window, cu_seqlens=cu,
+                                  max_seqlen=max(lengths), err_flag=err)
+    binding.check_err_flag(err)
+    cul = cu.cpu().tolist()
+    want_o, want_lse = oracle.sdpa_varlen(q.cpu(), k.cpu(), w["v"].cpu(), cul, cul, causal=True,
+                                          window=window)
+    assert T == cul[-1]
+    assert float(np.abs(want_lse).max()) > 60.0
+    assert_close_bf16(o, want_o, "o")
+    assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
 
 
 @pytest.mark.parametrize("hq,hkv,d", [(4, 2, 64), (8, 8, 128)])
