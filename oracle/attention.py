@@ -27,7 +27,7 @@ Definitions followed
   matching update of O -- "Ли Хунъи ... 2026", lecture "Ускоряем генерацию,
   часть 1: FlashAttention", the two displayed formulas.
 
-Readings where the pages are silent (also listed in the design doc):
+Readings where the pages are silent:
 * LSE is the natural log of the sum of exp(scaled score) over visible keys:
   lse = m + ln(l), one value per (query row, query head).
 * A query with no visible key (only possible when a sequence has no keys) gets
