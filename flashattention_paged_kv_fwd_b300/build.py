@@ -36,7 +36,7 @@ def sources():
 def deps():
     return sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) +
                               glob.glob(os.path.join(CSRC, "*.h")) +
-                              [os.path.join(ROOT, "include", "pagedattn.h")])
+                              glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def up_to_date():

@@ -54,12 +54,17 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
   if (cu_new == nullptr) {
     b = t;
     first = t;
-  } else if (staged) {
-    b = find_sequence(cu_s, n_seq, t);
-    first = cu_s[b];
   } else {
-    b = find_sequence(cu_new, n_seq, t);
-    first = cu_new[b];
+    const int32_t* cu = staged ? cu_s : cu_new;
+    // a token outside [cu[0], cu[n_seq]) belongs to no sequence: the offsets
+    // disagree with the token count, and guessing a sequence would overwrite
+    // another token's slot
+    if (t < cu[0] || t >= cu[n_seq]) {
+      if (lane == 0) raise_err(err, kDevErrBadPosition);
+      return;
+    }
+    b = find_sequence(cu, n_seq, t);
+    first = cu[b];
   }
   const int pos = seq_lens[b] + (t - first);
   const int lblk = pos / block_size;

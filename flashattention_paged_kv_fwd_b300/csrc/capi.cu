@@ -5,6 +5,7 @@
 // returns an error without touching the device. The library keeps no state
 // besides the cached driver entry point for cuTensorMapEncodeTiled, the SM
 // count per device and the per-kernel shared-memory attribute flags.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -12,12 +13,27 @@
 #include <cuda_runtime.h>
 
 #include "../../include/pagedattn.h"
+#include "../../include/pagedattn_testing.h"
 #include "host_util.h"
 #include "pa_kernels.h"
 
 using namespace pa::host;
 
+namespace pa {
+namespace {
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
+}  // namespace
+
+unsigned long long role_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+}  // namespace pa
+
 extern "C" {
+
+unsigned long long pa_testing_set_wait_limit_ns(unsigned long long ns) {
+  const unsigned long long v = (ns == 0 || ns > pa::kDefaultWaitNs) ? pa::kDefaultWaitNs : ns;
+  return pa::g_wait_limit_ns.exchange(v, std::memory_order_relaxed);
+}
 
 const char* pa_status_str(int status) {
   switch (status) {
@@ -56,6 +72,7 @@ int pa_attn_prefill(const void* q, const void* k, const void* v, void* o, float*
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.N = N; a.T = static_cast<int>(T); a.d = d;
   a.max_seqlen = msl; a.causal = causal ? 1 : 0; a.window = window > 0 ? window : 0;
   a.scale_log2 = scale_log2(scale, d);
+  a.wait_ns = pa::role_wait_limit_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (dtype == PA_F32) {
@@ -99,6 +116,7 @@ int pa_attn_prefill_paged(const void* q, const void* k_cache, const void* v_cach
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.N = total_q; a.T = total_q; a.d = d;
   a.max_seqlen = max_seqlen_q; a.causal = causal ? 1 : 0; a.window = window > 0 ? window : 0;
   a.scale_log2 = scale_log2(scale, d);
+  a.wait_ns = pa::role_wait_limit_ns();
   a.table = block_table; a.seq_lens_k = seq_lens;
   a.max_blocks = max_blocks_per_seq; a.num_blocks = num_blocks;
   CUtensorMap qm, km, vm;
@@ -209,6 +227,7 @@ int pa_attn_decode_paged(const void* q, const void* k_cache, const void* v_cache
   a.max_blocks = max_blocks_per_seq; a.num_blocks = num_blocks; a.B = B; a.Hq = Hq;
   a.Hkv = Hkv; a.d = d; a.window = window > 0 ? window : 0;
   a.scale_log2 = scale_log2(scale, d);
+  a.wait_ns = pa::role_wait_limit_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (f32) {

@@ -12,12 +12,17 @@
 //
 // The array is a file-scope __device__ variable of PA_NOALLOC_SCRATCH_BYTES:
 // every GPU that loads the library holds it until the process exits. From host
-// code its name is only a host-side stand-in, so the device address is looked
-// up once per device with cudaGetSymbolAddress and cached.
-#include <atomic>
+// code its name is only a host-side stand-in, so its device address is looked
+// up with cudaGetSymbolAddress on the first call in a context and cached per
+// device together with that context's unique id. A call from another context
+// of the device, or from the context that replaced a reset one (the module and
+// its array are loaded anew there, possibly at another address), finds a
+// different id and looks the address up again.
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "../../include/pagedattn.h"
 
@@ -26,21 +31,59 @@ namespace {
 static __device__ __align__(256) unsigned char g_decode_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
 
-// Device address of g_decode_scratch on the current device (looked up on the
-// first call for that device), or nullptr if the lookup failed.
+struct ScratchEntry {
+  unsigned long long ctx_id;  // unique id of the context the lookup was made in (0 = none)
+  void* addr;
+};
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  return nullptr;
+}
+
+// Unique id of the calling thread's current context (ids are never reused
+// within a process), or 0 when it cannot be read.
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_decode_scratch in the current context of the current
+// device, or nullptr if the lookup failed.
 void* scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();  // leave no sticky error from a failed lookup behind
-      return nullptr;
-    }
-    g_scratch_addr[dev].store(p, std::memory_order_release);
+  const unsigned long long id = current_context_id();  // 0 before the thread has a context
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  ScratchEntry& e = g_scratch[dev];
+  if (id != 0 && e.ctx_id == id && e.addr != nullptr) return e.addr;
+  void* p = nullptr;
+  // (this also makes the device's primary context current if none was)
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();  // leave no sticky error from a failed lookup behind
+    return nullptr;
   }
+  const unsigned long long now = id != 0 ? id : current_context_id();
+  // without a context id nothing is cached: every call looks the address up
+  e.ctx_id = now;
+  e.addr = now != 0 ? p : nullptr;
   return p;
 }
 

@@ -142,7 +142,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
       uint32_t valid_mask = 0;  // validity of the last `ns` issued blocks (bit per stage)
       for (int i = 0; i < npg; ++i) {
         const int st = i % ns, u = i / ns;
-        if (u > 0 && !mbar_wait(empty(st), (u - 1) & 1)) {
+        if (u > 0 && !mbar_wait(empty(st), (u - 1) & 1, a.wait_ns)) {
           raise_err(a.err, kDevErrTimeout);
           *abort_s = 1;
           break;
@@ -212,8 +212,9 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
 
   for (int i = 0; i < npg; ++i) {
     const int st = i % ns;
-    if (!mbar_wait(full(st), (i / ns) & 1)) {
-      raise_err(a.err, kDevErrTimeout);
+    // warp-uniform outcome: the ldmatrix / mma.sync below need all 32 lanes
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(full(st), (i / ns) & 1, a.wait_ns))) {
+      if (lane == 0) raise_err(a.err, kDevErrTimeout);
       *abort_s = 1;
       break;
     }

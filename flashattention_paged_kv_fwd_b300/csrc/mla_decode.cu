@@ -222,7 +222,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap cmap, const MlaArgs a, con
 
   for (int i = 0; i < nsteps; ++i) {
     const int st = i % ns;
-    const bool got = mbar_wait(full(st), (i / ns) & 1);
+    // warp-uniform: the ldmatrix / mma.sync below need all 32 lanes
+    const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(full(st), (i / ns) & 1));
     if (!got && lane == 0) {
       raise_err(a.err, kDevErrTimeout);
       *abort_s = 1;

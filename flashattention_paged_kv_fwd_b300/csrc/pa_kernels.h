@@ -8,6 +8,11 @@
 
 namespace pa {
 
+// Give-up limit (ns) of the waits between the roles of the prefill and decode
+// kernels: 2 s, unless a test shortened it (pa_testing_set_wait_limit_ns).
+// Waits for copies and MMAs already in flight keep their own limits.
+unsigned long long role_wait_limit_ns();
+
 // ------------------------------------------------------------------ append
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int32_t* table, int max_blocks, const int32_t* seq_lens,
@@ -53,6 +58,7 @@ struct DecodeArgs {
   int32_t* err;
   int max_blocks, num_blocks, B, Hq, Hkv, d, window;
   float scale_log2;
+  unsigned long long wait_ns;  // give-up limit of the pipeline waits (role_wait_limit_ns())
 };
 
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodePlan& p, const CUtensorMap& kmap,
@@ -80,6 +86,7 @@ struct PrefillArgs {
   const int32_t* table;       // nullptr => contiguous keys (rows of k / v)
   const int32_t* seq_lens_k;
   int max_blocks, num_blocks;
+  unsigned long long wait_ns;  // give-up limit of the pipeline waits (role_wait_limit_ns())
 };
 
 // Work units of the bf16 prefill (two 128-row query tiles each).

@@ -234,8 +234,10 @@ __device__ __forceinline__ int unit_of(int k, int c, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// Bounded wait (limit_ns of wall time) that also gives up as soon as another
+// role has aborted.
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -243,7 +245,7 @@ __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile 
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       return false;
     }
@@ -254,8 +256,8 @@ __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile 
 // give-up seen by one lane ends the loops of all 32 together (the warp-wide
 // tcgen05 and shuffle instructions that follow need every lane).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag) {
-  const bool ok = pf_wait(bar, parity, abort_flag);
+                                          volatile int* abort_flag, uint64_t limit_ns) {
+  const bool ok = pf_wait(bar, parity, abort_flag, limit_ns);
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
@@ -373,7 +375,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
     int q_loads = 0;            // units whose Q tiles were issued
     bool ok = true;
     auto load_tile = [&](const CUtensorMap* m, int row, int head) -> bool {
-      if (issued >= C::NSLOT && !warp_wait(bar(C::B_EMPTY + slot), phase ^ 1u, abort_flag))
+      if (issued >= C::NSLOT && !warp_wait(bar(C::B_EMPTY + slot), phase ^ 1u, abort_flag, a.wait_ns))
         return false;
       if (leader) {
         const uint32_t fb = bar(C::B_FULL + slot);
@@ -394,7 +396,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
     // block t (one 16-row box per 64-column panel) straight to its rows of
     // the slot. Blocks past the sequence's keys are not loaded.
     auto load_tile_paged = [&](const CUtensorMap* m, int key0, const Unit& w) -> bool {
-      if (issued >= C::NSLOT && !warp_wait(bar(C::B_EMPTY + slot), phase ^ 1u, abort_flag))
+      if (issued >= C::NSLOT && !warp_wait(bar(C::B_EMPTY + slot), phase ^ 1u, abort_flag, a.wait_ns))
         return false;
       const int pg = key0 / 16 + lane;
       bool have = lane < BN / 16 && pg * 16 < w.lk;
@@ -441,7 +443,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
           // the first K/V tiles go out before the Q tiles, which wait for the
           // previous unit's last QK^T
           for (int i = 0; i < 2 && ok; ++i) {
-            if (q_loads > 0 && !warp_wait(bar(C::B_QFREE + i), (q_loads - 1) & 1, abort_flag)) {
+            if (q_loads > 0 && !warp_wait(bar(C::B_QFREE + i), (q_loads - 1) & 1, abort_flag, a.wait_ns)) {
               ok = false;
               break;
             }
@@ -492,7 +494,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
     int uc = 0, tc = 0;
     bool ok = true;
     auto wait_full = [&](uint32_t& s) -> bool {
-      if (!warp_wait(bar(C::B_FULL + fslot), fphase, abort_flag)) return false;
+      if (!warp_wait(bar(C::B_FULL + fslot), fphase, abort_flag, a.wait_ns)) return false;
       s = fslot;
       if (++fslot == C::NSLOT) {
         fslot = 0;
@@ -521,10 +523,10 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       const uint32_t o_tm = tmem + C::TM_O + static_cast<uint32_t>(i * D);
       const uint32_t p_tm = tmem + static_cast<uint32_t>(i * BN);
       const uint64_t vd = dv + ((vs * C::TB) >> 4);
-      if (!warp_wait(bar(C::B_PRDY + 2 * i), tc & 1, abort_flag)) return false;
+      if (!warp_wait(bar(C::B_PRDY + 2 * i), tc & 1, abort_flag, a.wait_ns)) return false;
       tc_fence_after();
       umma_ts_k64keys_elect(o_tm, p_tm, vd, idesc_pv, acc);
-      if (!warp_wait(bar(C::B_PRDY + 2 * i + 1), tc & 1, abort_flag)) return false;
+      if (!warp_wait(bar(C::B_PRDY + 2 * i + 1), tc & 1, abort_flag, a.wait_ns)) return false;
       tc_fence_after();
       umma_ts_k64keys_elect(o_tm, p_tm + 32, vd + 512, idesc_pv, 1u);
       return true;
@@ -538,11 +540,11 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       if (!decode_unit(a, lv, sb, pr, w)) continue;
       const int n = w.n_tiles;
       uint32_t ks = 0, vs = 0;
-      if (!(ok = warp_wait(bar(C::B_QFULL + 0), uc & 1, abort_flag) && wait_full(ks))) break;
+      if (!(ok = warp_wait(bar(C::B_QFULL + 0), uc & 1, abort_flag, a.wait_ns) && wait_full(ks))) break;
       tc_fence_after();
       qk(0, ks);
       if (n == 1) commit(C::B_QFREE + 0);
-      if (!(ok = warp_wait(bar(C::B_QFULL + 1), uc & 1, abort_flag))) break;
+      if (!(ok = warp_wait(bar(C::B_QFULL + 1), uc & 1, abort_flag, a.wait_ns))) break;
       tc_fence_after();
       qk(1, ks);
       release();  // K(0)
@@ -613,7 +615,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       const int p0 = w.qoff + q0;          // position of the tile's first row
       float m = kNegInf, l = 0.f;
       for (int j = 0; j < w.n_tiles; ++j, ++tc) {
-        if (!(ok = warp_wait(bar(C::B_SFULL + ti), tc & 1, abort_flag))) break;
+        if (!(ok = warp_wait(bar(C::B_SFULL + ti), tc & 1, abort_flag, a.wait_ns))) break;
         tc_fence_after();
         uint32_t sr[BN];
 #pragma unroll
@@ -706,7 +708,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       }
       if (!ok) break;
-      if (!(ok = warp_wait(bar(C::B_OFULL + ti), uc & 1, abort_flag))) break;
+      if (!(ok = warp_wait(bar(C::B_OFULL + ti), uc & 1, abort_flag, a.wait_ns))) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int h = w.h[ti];

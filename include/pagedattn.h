@@ -33,8 +33,11 @@
  * Conventions shared by every call:
  *  - All pointers are DEVICE pointers except where stated; all tensors are
  *    dense and row-major in the index order given; the caller owns every
- *    buffer. The library never allocates device memory and keeps no state
- *    between calls (it caches one driver entry point and the SM count).
+ *    buffer. The library never allocates device memory. Its state between
+ *    calls is host-side caches (driver entry points, the SM count, kernel
+ *    attribute flags) plus one device-side array: the fixed scratch of
+ *    pa_attn_decode_paged_noalloc (PA_NOALLOC_SCRATCH_BYTES per GPU, part of
+ *    the loaded module), which only that entry point uses.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy stream).
  *  - Return value: PA_OK, or a host-detected error (nothing is launched).
  *  - err_flag (optional, may be NULL): an int32 in device memory that kernels
@@ -366,7 +369,11 @@ PA_API size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int max_b
  *    no scratch at all).
  *  - The first call on a device looks up the scratch's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture. PA_ERR_CUDA if the lookup fails.
+ *    before any stream capture. PA_ERR_CUDA if the lookup fails. The address
+ *    is cached per device with the unique id of the context it was looked up
+ *    in; the first call from another context of the device, or after
+ *    cudaDeviceReset replaced the context, looks it up again (so that call,
+ *    too, belongs before any capture).
  *  - All calls on a device share the one array, which keeps whatever the last
  *    call left there (nothing in it needs to start at zero). Calls that can
  *    overlap on the GPU -- on different streams, or from different host

@@ -3,6 +3,7 @@ every entry point the header declares, and rejects invalid arguments on the
 host before making any CUDA call."""
 
 import ctypes
+import glob
 import os
 import re
 import subprocess
@@ -13,7 +14,7 @@ from flashattention_paged_kv_fwd_b300 import build as pa_build
 from flashattention_paged_kv_fwd_b300 import binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE = 0, 1, 2, 4
 FAKE = 0x10000  # an aligned address that is never dereferenced (checks fail first)
@@ -26,7 +27,7 @@ def lib():
 
 
 def declared_symbols():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"PA_API[^;(]*?\b(pa_\w+)\s*\(", text)))
 
 
@@ -36,7 +37,7 @@ def test_header_declares_the_entry_points():
                  "pa_copy_blocks", "pa_attn_decode_paged", "pa_decode_workspace_bytes",
                  "pa_attn_prefill_backward", "pa_attn_prefill_backward_workspace_bytes",
                  "pa_mla_decode_paged", "pa_mla_decode_workspace_bytes", "pa_mla_append_paged",
-                 "pa_status_str"):
+                 "pa_status_str", "pa_attn_decode_paged_noalloc", "pa_testing_set_wait_limit_ns"):
         assert name in syms
 
 
@@ -265,3 +266,15 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         binding.load_library()
+
+
+def test_testing_wait_limit_hook_is_host_only_and_clamped(lib):
+    fn = lib.pa_testing_set_wait_limit_ns
+    fn.argtypes = [ctypes.c_ulonglong]
+    fn.restype = ctypes.c_ulonglong
+    default = 2_000_000_000
+    assert fn(1000) == default
+    assert fn(5 * default) == 1000      # above the default: back to the default
+    assert fn(7) == default
+    assert fn(0) == 7                   # 0 restores the default
+    assert fn(0) == default

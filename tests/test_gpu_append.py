@@ -110,3 +110,35 @@ def test_append_mixed_batch_full_size():
     keep = ~written[sb, so]
     assert torch.equal(bits(kc[sb[keep], so[keep]]), bits(w["k_cache"][sb[keep], so[keep]]))
     assert torch.equal(bits(vc[sb[keep], so[keep]]), bits(w["v_cache"][sb[keep], so[keep]]))
+
+
+@pytest.mark.parametrize("n_seq", [2, 5000])
+def test_append_flags_tokens_outside_cu_new(n_seq):
+    """cu_new that disagrees with the token count: tokens before cu_new[0] or
+    at/after cu_new[B] belong to no sequence. They are reported as a bad
+    position and not written anywhere; the tokens inside the offsets land
+    exactly where the oracle puts them. 5000 sequences exceed the offsets the
+    kernel stages in shared memory, so the check runs on the global array."""
+    before = [3, 20] + [0] * (n_seq - 2)
+    new = [3, 3] + [0] * (n_seq - 2)
+    c = inputs.make_paged_cache([b + n for b, n in zip(before, new)], before, 2, 64,
+                                torch.bfloat16, 41, "cuda", spare_blocks=2)
+    gen = inputs.make_generator(42, "cuda")
+    k_new = inputs.randn((10, 2, 64), torch.bfloat16, gen, "cuda")
+    v_new = inputs.randn((10, 2, 64), torch.bfloat16, gen, "cuda")
+    # tokens 0-1 and 8-9 lie outside every sequence's range
+    cu = [2, 5] + [8] * (n_seq - 1)
+    seq_lens = torch.tensor(before, dtype=torch.int32, device="cuda")
+    cu_new = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    kc, vc = c["k_cache"].clone(), c["v_cache"].clone()
+    err = binding.new_err_flag()
+    binding.kv_append_paged(k_new, v_new, kc, vc, c["block_table"], seq_lens, cu_new=cu_new,
+                            err_flag=err)
+    with pytest.raises(binding.PagedAttnError, match="position"):
+        binding.check_err_flag(err)
+    want_k, want_v = oracle.append_paged(c["k_cache"].cpu(), c["v_cache"].cpu(),
+                                         k_new[2:8].cpu(), v_new[2:8].cpu(),
+                                         c["block_table"][:2].cpu().tolist(), before[:2],
+                                         [0, 3, 6], 16)
+    assert torch.equal(bits(kc.cpu()), bits(want_k))
+    assert torch.equal(bits(vc.cpu()), bits(want_v))

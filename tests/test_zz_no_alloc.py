@@ -1,5 +1,6 @@
 """The decode entry point that allocates nothing (pa_attn_decode_paged_noalloc),
-called through the C ABI and compared with the regular decode entry point.
+called through the C ABI and compared with the oracle (naive block-table walk,
+fp64 softmax) and with the regular decode entry point.
 
 It serves callers that cannot allocate device memory when they call the
 library -- a serving process that reserves its memory at start-up and must not
@@ -13,6 +14,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from flashattention_paged_kv_fwd_b300 import binding, inputs
 from helpers import LSE_TOL, assert_close, assert_close_bf16
 
@@ -74,6 +76,12 @@ def test_noalloc_matches_regular_decode_on_two_calls_in_a_row(noalloc):
                                                      window=window, num_splits=splits)
         assert_close_bf16(out, want_o, f"call {n}: o")
         assert_close(lse.cpu(), want_lse.cpu(), f"call {n}: lse", LSE_TOL)
+        ref_o, ref_lse = oracle.decode_paged(w["q"].cpu(), w["k_cache"].cpu(),
+                                             w["v_cache"].cpu(), w["block_table"].cpu().tolist(),
+                                             w["seq_lens"].cpu().tolist(), block_size=16,
+                                             window=window)
+        assert_close_bf16(out, ref_o, f"call {n}: o vs oracle")
+        assert_close(lse.cpu(), ref_lse, f"call {n}: lse vs oracle", LSE_TOL)
 
 
 def test_noalloc_rejects_calls_whose_partials_do_not_fit(noalloc):
