@@ -73,6 +73,8 @@ def parse():
                     help="batch of gqa_decode_llama3_70b (smaller for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-configuration lines of the default run")
     ap.add_argument("--soak-s", type=float, default=1.5,
                     help="untimed seconds of steps before the timed region, sampled for clocks")
     return ap.parse_args()
@@ -556,6 +558,102 @@ def time_steps(run_phase, phases, n, flush, stream):
     return out
 
 
+# the other configurations, timed after the mixed step in the default run:
+# the GPT-2 / Llama-3-70B decodes and the Llama-3-8B prefill, then the
+# chunked prefill, backward, MLA decode and copy-on-write workloads
+EXTRA_WORKLOADS = ("mha_decode_gpt2", "gqa_prefill_llama3_8b", "gqa_decode_llama3_70b",
+                   "chunked_prefill_llama3_8b", "gqa_prefill_backward_llama3_8b",
+                   "mla_decode_deepseek_v2", "cow_copy_blocks_llama3_8b")
+
+PHASE_KERNEL = {"prefill": "prefill_bf16", "append": "kv_append", "decode": "decode_bf16",
+                "copy": "copy_blocks", "backward": "prefill_backward", "mla": "mla_decode"}
+
+
+def phase_rate(phase, work, ms, world):
+    """(value, unit) of one phase: TFLOP/s for the contractions, GB/s else."""
+    if phase in ("prefill", "backward"):
+        return whole_job_rate(work, world, ms) / 1e12, "TFLOP/s"
+    return whole_job_rate(work, world, ms) / 1e9, "GB/s"
+
+
+def phase_work(st, phase):
+    return {"prefill": st.flops, "backward": st.flops, "decode": st.dbytes, "mla": st.dbytes,
+            "copy": getattr(st, "cbytes", 0.0), "append": getattr(st, "abytes", 0.0)}[phase]
+
+
+def roofline_of(phase, achieved, peaks, peak_src, workload):
+    if phase in ("prefill", "backward"):
+        r = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+             "unit": "TFLOP/s"}
+    else:
+        r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" \
+        else "fallback (recipe)"
+    r["traffic"] = recorded_traffic(PHASE_KERNEL[phase], workload)
+    return r
+
+
+def time_workloads(names, args, dev, binding, flush, stream, world, peaks, peak_src):
+    """Each configuration on its own: W warm-up steps, then K timed steps with
+    the L2 flushed before each (CUDA events on the launching stream)."""
+    out = {}
+    for name in names:
+        st = SingleStep(name, dev, binding, args.decode_batch)
+        call = lambda ph: st.run()  # noqa: E731
+        time_steps(call, [st.phase], args.warmup, flush, stream)
+        t_soak = time.time()  # untimed, so that the clock samples see this kernel running
+        while time.time() - t_soak < min(args.soak_s, 0.4):
+            time_steps(call, [st.phase], 5, flush, stream)
+        t = time_steps(call, [st.phase], args.steps, flush, stream)[st.phase]
+        binding.check_err_flag(st.err)
+        ms = sum(t) / len(t)
+        ms, _ = max_over_ranks({st.phase: ms}, ms, dev)
+        ms = ms[st.phase]
+        work = phase_work(st, st.phase)
+        value, unit = phase_rate(st.phase, work, ms, world)
+        out[name] = {"kernel_family": st.phase, "value": value, "unit": unit, "ms": ms,
+                     "ms_min": min(t), "work": work, "launches": args.steps * st.launches[st.phase],
+                     "roofline": roofline_of(st.phase, value / world, peaks, peak_src, name)}
+        del st, call
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
+def pinned_link_gbs(device, nbytes=256 * 1024 * 1024, reps=5):
+    """Host<->device copy bandwidth from pinned memory on this machine (best of
+    `reps`, CUDA events), the bound the end-to-end copies run against."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    res = {}
+    for name, dst, src in (("h2d_gbs", d, h), ("d2h_gbs", h, d)):
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        res[name] = nbytes / (best * 1e-3) / 1e9
+    del h, d
+    return res
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or None
+
+
 def run_ours(args):
     world, rank, local = dist_info()
     if world > 1:
@@ -608,63 +706,42 @@ def run_ours(args):
 
     # throughput per phase (whole job: all replicas' work over the slowest rank)
     phases_out = {}
-    if "prefill" in phase_ms:
-        tf = whole_job_rate(st.flops, world, phase_ms["prefill"]) / 1e12
-        phases_out["prefill"] = {"ms": phase_ms["prefill"], "value": tf, "unit": "TFLOP/s",
-                                 "work": st.flops, "launches": st.launches["prefill"]}
-    if "backward" in phase_ms:
-        tf = whole_job_rate(st.flops, world, phase_ms["backward"]) / 1e12
-        phases_out["backward"] = {"ms": phase_ms["backward"], "value": tf, "unit": "TFLOP/s",
-                                  "work": st.flops, "launches": st.launches["backward"]}
-    if "mla" in phase_ms:
-        gb = whole_job_rate(st.dbytes, world, phase_ms["mla"]) / 1e9
-        phases_out["mla"] = {"ms": phase_ms["mla"], "value": gb, "unit": "GB/s",
-                             "work": st.dbytes, "launches": st.launches["mla"]}
-    if "append" in phase_ms:
-        gb = whole_job_rate(st.abytes, world, phase_ms["append"]) / 1e9
-        phases_out["append"] = {"ms": phase_ms["append"], "value": gb, "unit": "GB/s",
-                                "work": st.abytes, "launches": st.launches["append"]}
-    if "copy" in phase_ms:
-        gb = whole_job_rate(st.cbytes, world, phase_ms["copy"]) / 1e9
-        phases_out["copy"] = {"ms": phase_ms["copy"], "value": gb, "unit": "GB/s",
-                              "work": st.cbytes, "launches": st.launches["copy"]}
-    if "decode" in phase_ms:
-        gb = whole_job_rate(st.dbytes, world, phase_ms["decode"]) / 1e9
-        phases_out["decode"] = {"ms": phase_ms["decode"], "value": gb, "unit": "GB/s",
-                                "work": st.dbytes, "launches": st.launches["decode"]}
+    for ph in PHASES:
+        if ph in phase_ms:
+            work = phase_work(st, ph)
+            value, unit = phase_rate(ph, work, phase_ms[ph], world)
+            phases_out[ph] = {"ms": phase_ms[ph], "value": value, "unit": unit, "work": work,
+                              "launches": st.launches[ph]}
 
     # roofline of the kernel with the largest share of the step
     dom = max(phase_ms, key=phase_ms.get)
     roof = {}
     for ph, info in phases_out.items():
-        if ph in ("prefill", "backward"):
-            peak = peaks["bf16_tflops"]
-            r = {"bound": "tensor", "achieved": info["value"] / world, "peak": peak,
-                 "unit": "TFLOP/s"}
-        else:
-            peak = peaks["hbm_gbs"]
-            r = {"bound": "hbm", "achieved": info["value"] / world, "peak": peak, "unit": "GB/s"}
-        r["frac"] = r["achieved"] / r["peak"]
-        r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" \
-            else "fallback (recipe)"
-        kname = {"prefill": "prefill_bf16", "append": "kv_append", "decode": "decode_bf16",
-                 "copy": "copy_blocks", "backward": "prefill_backward",
-                 "mla": "mla_decode"}[ph]
-        r["traffic"] = recorded_traffic(kname, args.workload)
+        r = roofline_of(ph, info["value"] / world, peaks, peak_src, args.workload)
         r["kernel_share"] = phase_ms[ph] / step_ms
         roof[ph] = r
 
     # end to end: the same calls from pinned host buffers, copies inside the region
     e2e = None
     if not args.no_e2e and args.workload == "mixed_window4096" and not args.only:
-        e2e = run_e2e(st, args, stream, flush, world)
+        e2e = run_e2e(st, args, stream, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and \
             args.workload == "mixed_window4096":
         r = oracle_sample(st.w, 12.0, True)
         cpu = {"value": r["decode_gbs"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
-               "sample": r["sample"], "prefill_tflops": r["prefill_tflops"]}
+               "cpu_model": cpu_model(), "sample": r["sample"],
+               "prefill_tflops": r["prefill_tflops"]}
+
+    # the other configurations, each timed on its own (same flush and events)
+    workloads = None
+    if args.workload == "mixed_window4096" and not args.only and not args.no_workloads:
+        sampler_w = ClockSampler(sampler.gpu)
+        sampler_w.start()
+        workloads = time_workloads(EXTRA_WORKLOADS, args, dev, binding, flush, stream, world,
+                                   peaks, peak_src)
+        workloads["clocks"] = sampler_w.stop()
 
     if args.workload == "mixed_window4096":
         head = "decode" if "decode" in phases_out else list(phases_out)[0]
@@ -710,6 +787,7 @@ def run_ours(args):
         "clocks": clocks,
         "gpu_launches": launches,
         "wall_s_timed_region": wall,
+        "workloads": workloads,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -718,14 +796,20 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(st, args, stream, flush, world):
+def run_e2e(st, args, stream, world):
     """End to end through the public API: every step copies its inputs host
     -> device from pinned memory, makes the three calls and copies the outputs
-    device -> host. Steps are pipelined over three streams (inputs of step
-    i+1 and outputs of step i-1 move while step i computes), with two sets of
-    device input and output buffers; all K steps' copies and calls lie between
-    the two events. The step inputs (322 MB) exceed L2, so no flush is needed
-    between steps."""
+    device -> host; all copies and calls lie between the two events. The step
+    inputs (322 MB) exceed L2, so no flush is needed between steps.
+
+    Two schedules are timed:
+    * serial: one step at a time on one stream (copy in, compute, copy out),
+      the latency of a step;
+    * pipelined: steps over three streams with two sets of device input and
+      output buffers (the inputs of step i+1 and the outputs of step i-1 move
+      while step i computes), the throughput. ``value`` is this one.
+    The box's pinned host<->device bandwidth is measured beside them, so the
+    copies' share of a step can be judged against the link."""
     w = st.w
     pre = w["prefill"]
     device = w["q_dec"].device
@@ -746,6 +830,31 @@ def run_e2e(st, args, stream, flush, world):
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
+    def compute(b):
+        st.o_pre, st.lse_pre = dev_out[b]["o_pre"], dev_out[b]["lse_pre"]
+        st.o_dec, st.lse_dec = dev_out[b]["o_dec"], dev_out[b]["lse_dec"]
+        d = dev[b]
+        T = st.T
+        st.prefill(d["q"], d["k_new"][:T], d["v_new"][:T], d["cu"])
+        st.append(d["k_new"], d["v_new"], d["seq_before"], d["cu_new"], d["table"])
+        st.decode(d["q_dec"], d["seq_dec"], d["table"][st.npf:])
+
+    def serial(n):
+        marks = []
+        for _ in range(n):
+            a = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k in host:
+                dev[0][k].copy_(host[k], non_blocking=True)
+            compute(0)
+            for k in outs:
+                outs[k].copy_(dev_out[0][k], non_blocking=True)
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            marks.append((a, e))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(e) for a, e in marks]
+
     def pipeline(n, start=None):
         in_ready, done, copied = [], [], []
         for i in range(n):
@@ -763,13 +872,7 @@ def run_e2e(st, args, stream, flush, world):
             stream.wait_event(in_ready[i])
             if i >= 2:
                 stream.wait_event(copied[i - 2])  # dev_out[b] has been copied out
-            st.o_pre, st.lse_pre = dev_out[b]["o_pre"], dev_out[b]["lse_pre"]
-            st.o_dec, st.lse_dec = dev_out[b]["o_dec"], dev_out[b]["lse_dec"]
-            d = dev[b]
-            T = st.T
-            st.prefill(d["q"], d["k_new"][:T], d["v_new"][:T], d["cu"])
-            st.append(d["k_new"], d["v_new"], d["seq_before"], d["cu_new"], d["table"])
-            st.decode(d["q_dec"], d["seq_dec"], d["table"][st.npf:])
+            compute(b)
             e = torch.cuda.Event()
             e.record(stream)
             done.append(e)
@@ -782,6 +885,9 @@ def run_e2e(st, args, stream, flush, world):
                 copied.append(e)
         return copied[-1]
 
+    serial(max(3, args.warmup))
+    t_serial = serial(args.steps)
+    ms_serial = sum(t_serial) / len(t_serial)
     pipeline(max(2, args.warmup))
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
@@ -789,11 +895,18 @@ def run_e2e(st, args, stream, flush, world):
     end = pipeline(args.steps, start)
     end.synchronize()
     torch.cuda.synchronize()
-    step = start.elapsed_time(end) / args.steps
-    return {"value": world * st.dbytes / (step * 1e-3) / 1e9, "unit": "GB/s",
+    ms_pipe = start.elapsed_time(end) / args.steps
+    link = pinned_link_gbs(device)
+    # with both directions overlapped, the copies alone bound a step at the
+    # slower of the two; serialised, at their sum
+    link["copy_ms_overlapped"] = max(h2d / (link["h2d_gbs"] * 1e6), d2h / (link["d2h_gbs"] * 1e6))
+    link["copy_ms_serial"] = h2d / (link["h2d_gbs"] * 1e6) + d2h / (link["d2h_gbs"] * 1e6)
+    return {"value": world * st.dbytes / (ms_pipe * 1e-3) / 1e9, "unit": "GB/s",
             "basis": "decode KV bytes / whole step time (copies + prefill + append + decode, "
                      "steps pipelined over three streams)",
-            "ms_per_step": step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step_pipelined": ms_pipe, "ms_per_step_serial": ms_serial,
+            "value_serial": world * st.dbytes / (ms_serial * 1e-3) / 1e9,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "pinned_link": link}
 
 
 def main():

@@ -44,18 +44,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase: never suspends the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Every wait in this library is bounded: after `limit_ns` of wall time the
 // wait gives up and returns false; the caller records an error and unwinds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// try_wait may suspend the thread until the phase completes, so a wait made
+// of try_waits only looks at the clock when a whole run of them failed. A
+// limit below this one (set only by tests of the give-up path) is polled
+// with test_wait instead, which returns at once, and the clock is read every
+// few polls, so a short limit really ends the wait.
+constexpr uint64_t kQuickPollBelowNs = 1000000ull;  // 1 ms
+
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, bool quick) {
+  return quick ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool quick = limit_ns < kQuickPollBelowNs;
+  const int spins = quick ? 4 : 256;  // polls between clock reads
+  if (mbar_poll(bar, parity, quick)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < spins; ++i)
+      if (mbar_poll(bar, parity, quick)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }

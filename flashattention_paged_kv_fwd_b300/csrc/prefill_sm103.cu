@@ -238,12 +238,14 @@ __device__ __forceinline__ int unit_of(int k, int c, int G) {
 // role has aborted.
 __device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                         uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool quick = limit_ns < kQuickPollBelowNs;  // a test's short limit
+  const int spins = quick ? 4 : 64;                  // polls between clock reads
+  if (mbar_poll(bar, parity, quick)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < spins; ++i)
+      if (mbar_poll(bar, parity, quick)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;

@@ -28,9 +28,12 @@ extern "C" {
  * the kernels that pa_attn_prefill, pa_attn_prefill_paged and
  * pa_attn_decode_paged (and its no-allocation variant) launch from now on in
  * this process, and returns the previous limit. 0, or anything above the
- * default of 2 s, restores the default. The waits for copies and MMAs already
- * in flight keep their own limit (0.1 s). Host-only: it touches no device and
- * affects launches made after it returns; set it back before other work.
+ * default of 2 s, restores the default. Under a limit below 1 ms the waits
+ * poll without suspending the waiting threads and read the clock every few
+ * polls, so that the limit is seen soon after it runs out. The waits for copies and
+ * MMAs already in flight keep their own limit (0.1 s). Host-only: it touches
+ * no device and affects launches made after it returns; set it back before
+ * other work.
  */
 PA_API unsigned long long pa_testing_set_wait_limit_ns(unsigned long long ns);
 
