@@ -18,30 +18,36 @@
 // same K/V stream: the same rows of two query heads of one KV group when
 // Hq/Hkv is even, otherwise two consecutive row tiles of one head (their key
 // ranges are merged; keys a tile may not see are masked).
-//  * warp 8 (TMA producer): the unit's two Q tiles, then K and V tiles of 128
-//    keys in turn through a ring of 32 KB slots (d = 128). Every tile is
-//    stored as 64-element (128-byte) panels, 128-byte swizzled: the K-major /
-//    MN-major operand layouts the tensor cores read directly.
-//  * warp 9 (tcgen05 issuer): MMAs in the steady order
+//  * warp 16 (K/V producer): K and V tiles of 128 keys in turn through a
+//    ring of 32 KB slots (d = 128). Every tile is stored as 64-element
+//    (128-byte) panels, 128-byte swizzled: the K-major / MN-major operand
+//    layouts the tensor cores read directly.
+//  * warp 18 (Q producer): the unit's two Q tiles, each as soon as the last
+//    QK^T of the previous unit on that tile has been issued. Apart from the
+//    K/V producer, so that the ring keeps filling across unit boundaries.
+//  * warp 17 (tcgen05 issuer): MMAs in the steady order
 //      ... QK_0(j), PV_1(j-1), QK_1(j), PV_0(j), QK_0(j+1), PV_1(j), ...
 //    S_i = Q_i K^T (M=128, N=128, both operands in shared memory) into TMEM,
 //    and O_i += P_i V (A = P_i read from TMEM, B = V in shared memory). Each
 //    softmax therefore has two other MMAs (about 1000 cycles) to run in, and
-//    the two softmax warpgroups take turns on the SFU. Descriptors are formed
+//    the two softmax groups take turns on the SFU. Descriptors are formed
 //    once; the per-MMA issue work is one add, which keeps the MMA pipe full.
-//  * warps 0-3 / 4-7 (softmax of query tile 0 / 1, one row per thread): read
-//    the row's 128 scores from TMEM, mask only on tiles that straddle the
-//    diagonal, the window edge or the sequence end, update the running max in
-//    the log2 domain with scale*log2(e) folded into one FMA, exponentiate with
-//    ex2, and write P as bf16 pairs back into the first 64 columns of the same
-//    TMEM score buffer, where the PV MMA reads it. At the end of a unit they
-//    read O from TMEM, divide by the running sum and store O and the LSE.
+//  * warps 0-7 / 8-15 (softmax of query tile 0 / 1): each warp owns 16 rows
+//    through the 16-lane TMEM access shapes, four threads per row. Per key
+//    tile and per half of 64 keys: read the scores from TMEM, mask only on
+//    tiles that straddle the diagonal, the window edge or the sequence end,
+//    reduce the rows' max over the quad with shuffles, update the running
+//    max in the log2 domain with scale*log2(e) folded into one FMA,
+//    exponentiate with ex2, write P as bf16 pairs back into the score
+//    buffer's first 64 columns, where the PV MMA reads it, and hand that
+//    half over. At the end of a unit they read O from TMEM, divide by the
+//    running sum and store O and the LSE.
 //  * The max is rescaled lazily: O and the sum are only rescaled when the max
 //    grows by more than 2^8; otherwise the stale max is kept. O / sum is
 //    unchanged (both carry the same factor), P stays <= 256, and TMEM round
-//    trips of O become rare. When a softmax sees S_i(j), the commit that
-//    signalled it also covers PV_i(j-1), so O_i is idle until P_i(j) is
-//    handed over and the rescale needs no extra wait.
+//    trips of O become rare. Before a tile's first hand-over O is idle (the
+//    commit that signalled S_i(j) also covers PV_i(j-1)); before the second,
+//    the rescale waits for the commit that follows the first PV half.
 //  * S_i(j+1) overwrites the TMEM columns that hold P_i(j). The MMA that
 //    reads P_i(j) is issued before the MMA that overwrites it, by the same
 //    thread, and the SM's tensor core executes one thread's MMAs in issue
@@ -71,9 +77,11 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max g
 
 constexpr int kMaxSchedSeqs = 512;  // packed sequences the on-chip work list can sort
 
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;  // 8 softmax warps + producer + MMA issuer
+constexpr int kSoftmaxWarps = 16;  // 8 per query tile
+constexpr int kLoadWarp = 16;      // K / V producer
+constexpr int kMmaWarp = 17;       // tcgen05 issuer
+constexpr int kQWarp = 18;         // Q producer
+constexpr int kThreads = 19 * 32;
 
 template <int D>
 struct PfCfg {
@@ -94,7 +102,8 @@ struct PfCfg {
   static constexpr int B_PRDY = 6 + 2 * NSLOT;    // + 2 * query tile + half (keys 0-63 / 64-127)
   static constexpr int B_OFULL = 10 + 2 * NSLOT;  // + query tile
   static constexpr int B_DRAIN = 12 + 2 * NSLOT;
-  static constexpr int NBAR = 13 + 2 * NSLOT;
+  static constexpr int B_PVH0 = 13 + 2 * NSLOT;   // + query tile: PV over keys 0-63 done
+  static constexpr int NBAR = 15 + 2 * NSLOT;
   static constexpr int OFF_SCHED = OFF_BAR + NBAR * 8 + 16;  // after the TMEM slot + abort flag
   static constexpr int SMEM = OFF_SCHED + 2 * kMaxSchedSeqs * 2 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -333,9 +342,10 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         mbar_init(bar(C::B_QFULL + i), 1);
         mbar_init(bar(C::B_QFREE + i), 1);
         mbar_init(bar(C::B_SFULL + i), 1);
-        mbar_init(bar(C::B_PRDY + 2 * i), 128);
-        mbar_init(bar(C::B_PRDY + 2 * i + 1), 128);
+        mbar_init(bar(C::B_PRDY + 2 * i), kSoftmaxWarps / 2 * 32);
+        mbar_init(bar(C::B_PRDY + 2 * i + 1), kSoftmaxWarps / 2 * 32);
         mbar_init(bar(C::B_OFULL + i), 1);
+        mbar_init(bar(C::B_PVH0 + i), 1);
       }
       for (int s = 0; s < C::NSLOT; ++s) {
         mbar_init(bar(C::B_FULL + s), 1);
@@ -368,13 +378,11 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
     // ------------------------------------------------------------ producer
     const bool leader = lane == 0;
     if (leader) {
-      prefetch_tmap(&qmap);
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
     }
     uint32_t slot = 0, phase = 0;
     int issued = 0;             // K/V tiles issued into the ring
-    int q_loads = 0;            // units whose Q tiles were issued
     bool ok = true;
     auto load_tile = [&](const CUtensorMap* m, int row, int head) -> bool {
       if (issued >= C::NSLOT && !warp_wait(bar(C::B_EMPTY + slot), phase ^ 1u, abort_flag, a.wait_ns))
@@ -441,27 +449,6 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
           ok = load_tile_paged(&kmap, key0, w) && load_tile_paged(&vmap, key0, w);
         else
           ok = load_tile(&kmap, w.start + key0, w.kvh) && load_tile(&vmap, w.start + key0, w.kvh);
-        if (ok && j == 0) {
-          // the first K/V tiles go out before the Q tiles, which wait for the
-          // previous unit's last QK^T
-          for (int i = 0; i < 2 && ok; ++i) {
-            if (q_loads > 0 && !warp_wait(bar(C::B_QFREE + i), (q_loads - 1) & 1, abort_flag, a.wait_ns)) {
-              ok = false;
-              break;
-            }
-            if (leader) {
-              const uint32_t qb = bar(C::B_QFULL + i);
-              mbar_arrive_expect_tx(qb, C::QB);
-#pragma unroll
-              for (int p = 0; p < D / 64; ++p)
-                tma_load_3d(sQ + i * C::QB + p * C::PANEL_Q, &qmap, qb, p * 64, w.h[i],
-                            w.start + w.q0[i]);
-            }
-            __syncwarp();
-          }
-          // counted once both were issued (a half-issued pair is drained below)
-          if (ok) ++q_loads;
-        }
       }
     }
     // every copy issued must land before the CTA exits
@@ -471,10 +458,47 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         const int p = issued - t;
         mbar_wait(bar(C::B_FULL + p % C::NSLOT), (p / C::NSLOT) & 1, kDrainLimitNs);
       }
-      if (!ok) {
-        // the pair of the unit being set up may be partly issued
-        mbar_wait(bar(C::B_QFULL + 0), q_loads & 1, kDrainLimitNs);
+      if (!ok) raise_err(a.err, kDevErrTimeout);
+    }
+  } else if (warp == kQWarp) {
+    // ---------------------------------------------------------- Q producer
+    // The two query tiles of each unit, each as soon as the MMA warp has
+    // issued the last QK^T of the previous unit on that tile. Kept apart
+    // from the K / V producer so that its ring runs on into the next unit
+    // while these wait.
+    const bool leader = lane == 0;
+    if (leader) prefetch_tmap(&qmap);
+    int q_loads = 0;  // units whose Q tiles were issued
+    int half = 0;     // tiles of the current unit issued (an abort may leave 1)
+    bool ok = true;
+    for (int k = 0; ok && k * G < n_units; ++k) {
+      const int u = unit_of(k, cta, G);
+      Unit w;
+      int lv, sb, pr;
+      if (u >= n_units) continue;
+      sched.map(u, lv, sb, pr);
+      if (!decode_unit(a, lv, sb, pr, w)) continue;
+      for (half = 0; half < 2; ++half) {
+        if (q_loads > 0 &&
+            !warp_wait(bar(C::B_QFREE + half), (q_loads - 1) & 1, abort_flag, a.wait_ns)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
+          const uint32_t qb = bar(C::B_QFULL + half);
+          mbar_arrive_expect_tx(qb, C::QB);
+#pragma unroll
+          for (int p = 0; p < D / 64; ++p)
+            tma_load_3d(sQ + half * C::QB + p * C::PANEL_Q, &qmap, qb, p * 64, w.h[half],
+                        w.start + w.q0[half]);
+        }
+        __syncwarp();
       }
+      if (ok) ++q_loads;
+    }
+    // every Q copy issued must land before the CTA exits
+    if (leader) {
+      if (!ok && half > 0) mbar_wait(bar(C::B_QFULL + 0), q_loads & 1, kDrainLimitNs);
       if (q_loads > 0) {
         mbar_wait(bar(C::B_QFULL + 0), (q_loads - 1) & 1, kDrainLimitNs);
         mbar_wait(bar(C::B_QFULL + 1), (q_loads - 1) & 1, kDrainLimitNs);
@@ -528,6 +552,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       if (!warp_wait(bar(C::B_PRDY + 2 * i), tc & 1, abort_flag, a.wait_ns)) return false;
       tc_fence_after();
       umma_ts_k64keys_elect(o_tm, p_tm, vd, idesc_pv, acc);
+      commit(C::B_PVH0 + i);  // a softmax that must rescale O before the second half waits for it
       if (!warp_wait(bar(C::B_PRDY + 2 * i + 1), tc & 1, abort_flag, a.wait_ns)) return false;
       tc_fence_after();
       umma_ts_k64keys_elect(o_tm, p_tm + 32, vd + 512, idesc_pv, 1u);
@@ -595,10 +620,20 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
     if (!ok && lane == 0) raise_err(a.err, kDevErrTimeout);
   } else {
     // ------------------------------------------------ softmax / epilogue
-    const int ti = warp >> 2;              // query tile of this warpgroup
-    const int wq = warp & 3;               // TMEM lane quarter of this warp
-    const int r = wq * 32 + lane;          // row of the query tile
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    // Eight warps per query tile. Warp (ti, q4, hh) owns the 16 rows q4*32 +
+    // hh*16 .. +15 of tile ti (TMEM lanes of its quarter q4) and reaches them
+    // with the 16-lane access shapes: thread t holds rows ra = t/4 and ra + 8
+    // of those, key columns 8r + 2(t%4) + {0, 1} for r = 0..15. The four
+    // threads of a quad share two rows; row max and sum are reduced with two
+    // shuffles. P for keys (8r + 2(t%4), +1) is one bf16 pair, which belongs
+    // in TMEM column 4r + t%4: exactly where the .16x128b store puts this
+    // thread's register, so every warp reads S and writes P in its own 16
+    // lanes only.
+    const int ti = warp >> 3;                         // query tile of this warp
+    const int q4 = warp & 3, hh = (warp >> 2) & 1;    // lane quarter, half of it
+    const int jq = lane & 3;                          // thread within the quad
+    const int ra = q4 * 32 + hh * 16 + (lane >> 2);   // row a of the tile; row b = ra + 8
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32 + hh * 16) << 16;
     const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(ti * BN);
     const uint32_t tO = tmem + lane_off + C::TM_O + static_cast<uint32_t>(ti * D);
     const float sl2 = a.scale_log2;
@@ -612,133 +647,184 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       sched.map(u, lv, sb, pr);
       if (!decode_unit(a, lv, sb, pr, w)) continue;
       const int q0 = w.q0[ti];
-      const int q_row = q0 + r;            // query row within its sequence
-      const int i_abs = w.qoff + q_row;    // its position among the keys
-      const int p0 = w.qoff + q0;          // position of the tile's first row
-      float m = kNegInf, l = 0.f;
+      const int qa = q0 + ra, qb = qa + 8;   // query rows within the sequence
+      const int ia = w.qoff + qa;            // their positions among the keys (ib = ia + 8)
+      const int p0 = w.qoff + q0;            // position of the tile's first row
+      float ma = kNegInf, mb = kNegInf, la = 0.f, lb = 0.f;
       for (int j = 0; j < w.n_tiles; ++j, ++tc) {
         if (!(ok = warp_wait(bar(C::B_SFULL + ti), tc & 1, abort_flag, a.wait_ns))) break;
         tc_fence_after();
-        uint32_t sr[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
-        tmem_wait_ld();
-
         const int kt0 = (w.t_begin + j) * BN;
         const bool need_mask = (kt0 + BN > w.lk) || (a.causal && kt0 + BN - 1 > p0) ||
                                (a.window > 0 && kt0 <= p0 + BM - 1 - a.window);
-        if (need_mask) {
-#pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            const int jk = kt0 + c;
-            const bool vis = jk < w.lk && (!a.causal || jk <= i_abs) &&
-                             (a.window <= 0 || jk > i_abs - a.window);
-            if (!vis) sr[c] = __float_as_uint(kNegInf);
-          }
-        }
-        // row max: 8 independent chains, three-input max
-        float mx8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float v = fmaxf(__uint_as_float(sr[e]), __uint_as_float(sr[e + 8]));
-#pragma unroll
-          for (int c = 16; c < BN; c += 16)
-            v = fmax3(v, __uint_as_float(sr[c + e]), __uint_as_float(sr[c + 8 + e]));
-          mx8[e] = v;
-        }
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                               fmaxf(mx8[6], mx8[7]));
-        const float m_new = fmaxf(m, mx * sl2);
-        const bool resc = m_new > m + kRescaleThreshold;
-        float alpha = 1.f;
-        if (resc) {
-          alpha = ex2(m - m_new);  // 0 when m = -inf
-          m = m_new;
-        }
-        l *= alpha;
-        const float m_use = m == kNegInf ? 0.f : m;
-        // p = 2^(s*scale*log2(e) - m) on pairs of scores: one packed FMA per
-        // pair, one ex2 per score, sums in 8 partials (4 packed accumulators).
-        // P goes to TMEM and is handed to the MMA warp in two halves of 64
-        // keys, so the first half of PV runs while the second is computed.
-        const uint64_t sl2x2 = f2(sl2, sl2), negm2 = f2(-m_use, -m_use);
-        uint64_t acc2[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc2[e] = 0ull;
+        // key column 8r + e + 2*jq of the tile is visible to a row iff
+        // lo <= 8r + e < hi (bounds shifted by this thread's 2*jq)
+        const int sh = kt0 + 2 * jq;
+        const int lim = w.lk - sh;
+        const int hia = a.causal ? min(lim, ia + 1 - sh) : lim;
+        const int hib = a.causal ? min(lim, ia + 9 - sh) : lim;
+        const int loa = a.window > 0 ? ia + 1 - a.window - sh : -BN;
+        const int lob = loa + 8;
+        const uint64_t sl2x2 = f2(sl2, sl2);
+        uint64_t sa[2] = {0ull, 0ull}, sb2[2] = {0ull, 0ull};
+        // Keys in two halves of 64. Each half: load its scores, take the
+        // rows' max over the quad, move the running max if it grew by more
+        // than 2^8 (lazy rescale, log2 domain), exponentiate, write P to TMEM
+        // and hand it to the MMA warp, so PV of the first half runs while the
+        // second is computed.
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          uint32_t pk[32];
+          uint32_t sr[32];
+          tmem_ld16x256_x8(tS + 64 * hf, sr);
+          tmem_wait_ld();
+          if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const uint64_t x = ffma2(f2(__uint_as_float(sr[64 * hf + 2 * e]),
-                                        __uint_as_float(sr[64 * hf + 2 * e + 1])),
-                                     sl2x2, negm2);
-            float x0, x1;
-            unf2(x, x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            acc2[e & 3] = fadd2(acc2[e & 3], f2(p0, p1));
-            pk[e] = pack_bf16(p0, p1);
-          }
-          tmem_st32(tS + 32 * hf, pk);
-          if (hf == 0 && j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
-            // O_i is idle here: PV_i(j-1) finished before S_i(j) was signalled
-            // and PV_i(j) waits for the first hand-over below
+            for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tO + 32 * c, o);
-              tmem_wait_ld();
-              const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                float lo, hi;
-                unf2(fmul2(f2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
-                o[e] = __float_as_uint(lo);
-                o[e + 1] = __float_as_uint(hi);
+              for (int e = 0; e < 2; ++e) {
+                const int c = 64 * hf + 8 * r + e;
+                if (c >= hia || c < loa) sr[4 * r + e] = __float_as_uint(kNegInf);
+                if (c >= hib || c < lob) sr[4 * r + 2 + e] = __float_as_uint(kNegInf);
               }
-              tmem_st32(tO + 32 * c, o);
+          }
+          float xa0 = fmaxf(__uint_as_float(sr[0]), __uint_as_float(sr[1]));
+          float xa1 = fmaxf(__uint_as_float(sr[4]), __uint_as_float(sr[5]));
+          float xb0 = fmaxf(__uint_as_float(sr[2]), __uint_as_float(sr[3]));
+          float xb1 = fmaxf(__uint_as_float(sr[6]), __uint_as_float(sr[7]));
+#pragma unroll
+          for (int r = 2; r < 8; r += 2) {
+            xa0 = fmax3(xa0, __uint_as_float(sr[4 * r]), __uint_as_float(sr[4 * r + 1]));
+            xa1 = fmax3(xa1, __uint_as_float(sr[4 * r + 4]), __uint_as_float(sr[4 * r + 5]));
+            xb0 = fmax3(xb0, __uint_as_float(sr[4 * r + 2]), __uint_as_float(sr[4 * r + 3]));
+            xb1 = fmax3(xb1, __uint_as_float(sr[4 * r + 6]), __uint_as_float(sr[4 * r + 7]));
+          }
+          float mxa = fmaxf(xa0, xa1), mxb = fmaxf(xb0, xb1);
+          mxa = fmaxf(mxa, __shfl_xor_sync(0xFFFFFFFFu, mxa, 1));
+          mxb = fmaxf(mxb, __shfl_xor_sync(0xFFFFFFFFu, mxb, 1));
+          mxa = fmaxf(mxa, __shfl_xor_sync(0xFFFFFFFFu, mxa, 2));
+          mxb = fmaxf(mxb, __shfl_xor_sync(0xFFFFFFFFu, mxb, 2));
+          const float mna = fmaxf(ma, mxa * sl2), mnb = fmaxf(mb, mxb * sl2);
+          const bool rsa = mna > ma + kRescaleThreshold, rsb = mnb > mb + kRescaleThreshold;
+          float ala = 1.f, alb = 1.f;
+          if (rsa) {
+            ala = ex2(ma - mna);  // 0 when ma = -inf
+            ma = mna;
+          }
+          if (rsb) {
+            alb = ex2(mb - mnb);
+            mb = mnb;
+          }
+          la *= ala;
+          lb *= alb;
+          if (hf == 1) {
+            // the first half's sums were taken with the old max
+            sa[0] = fmul2(sa[0], f2(ala, ala));
+            sa[1] = fmul2(sa[1], f2(ala, ala));
+            sb2[0] = fmul2(sb2[0], f2(alb, alb));
+            sb2[1] = fmul2(sb2[1], f2(alb, alb));
+          }
+          // O carries the same factor. Before the first hand-over of a tile
+          // O is idle (PV of the previous tile finished before S was
+          // signalled); before the second, PV of the first half may still
+          // run, so its completion is waited for. On a tile's first half of
+          // a unit's first tile O is about to be overwritten: nothing to do.
+          if ((hf == 1 || j > 0) && __any_sync(0xFFFFFFFFu, rsa || rsb)) {
+            if (hf == 1 && !(ok = warp_wait(bar(C::B_PVH0 + ti), tc & 1, abort_flag, a.wait_ns)))
+              break;
+            tc_fence_after();
+            const uint64_t a2 = f2(ala, ala), b2 = f2(alb, alb);
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t o[8];
+              tmem_ld16x256_x2(tO + 16 * c, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                float x0, x1;
+                unf2(fmul2(f2(__uint_as_float(o[4 * r]), __uint_as_float(o[4 * r + 1])), a2), x0,
+                     x1);
+                o[4 * r] = __float_as_uint(x0);
+                o[4 * r + 1] = __float_as_uint(x1);
+                unf2(fmul2(f2(__uint_as_float(o[4 * r + 2]), __uint_as_float(o[4 * r + 3])), b2),
+                     x0, x1);
+                o[4 * r + 2] = __float_as_uint(x0);
+                o[4 * r + 3] = __float_as_uint(x1);
+              }
+              tmem_st16x256_x2(tO + 16 * c, o);
             }
           }
+          // p = 2^(s*scale*log2(e) - m) on pairs of scores
+          const float mua = ma == kNegInf ? 0.f : ma, mub = mb == kNegInf ? 0.f : mb;
+          const uint64_t nma = f2(-mua, -mua), nmb = f2(-mub, -mub);
+          uint32_t pk[16];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            float p0a, p1a, p0b, p1b;
+            unf2(ffma2(f2(__uint_as_float(sr[4 * r]), __uint_as_float(sr[4 * r + 1])), sl2x2, nma),
+                 p0a, p1a);
+            unf2(ffma2(f2(__uint_as_float(sr[4 * r + 2]), __uint_as_float(sr[4 * r + 3])), sl2x2,
+                       nmb),
+                 p0b, p1b);
+            p0a = ex2(p0a);
+            p1a = ex2(p1a);
+            p0b = ex2(p0b);
+            p1b = ex2(p1b);
+            sa[r & 1] = fadd2(sa[r & 1], f2(p0a, p1a));
+            sb2[r & 1] = fadd2(sb2[r & 1], f2(p0b, p1b));
+            pk[2 * r] = pack_bf16(p0a, p1a);
+            pk[2 * r + 1] = pack_bf16(p0b, p1b);
+          }
+          tmem_st16x128_x8(tS + 32 * hf, pk);
           tmem_wait_st();
           tc_fence_before();
           mbar_arrive(bar(C::B_PRDY + 2 * ti + hf));
         }
-        float ls[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) unf2(acc2[e], ls[2 * e], ls[2 * e + 1]);
-        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        if (!ok) break;
+        float u0, u1, v0, v1;
+        unf2(fadd2(sa[0], sa[1]), u0, u1);
+        unf2(fadd2(sb2[0], sb2[1]), v0, v1);
+        la += u0 + u1;
+        lb += v0 + v1;
       }
       if (!ok) break;
       if (!(ok = warp_wait(bar(C::B_OFULL + ti), uc & 1, abort_flag, a.wait_ns))) break;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // the rows' sums over the whole quad
+      la += __shfl_xor_sync(0xFFFFFFFFu, la, 1);
+      lb += __shfl_xor_sync(0xFFFFFFFFu, lb, 1);
+      la += __shfl_xor_sync(0xFFFFFFFFu, la, 2);
+      lb += __shfl_xor_sync(0xFFFFFFFFu, lb, 2);
+      const float inva = la > 0.f ? 1.f / la : 0.f, invb = lb > 0.f ? 1.f / lb : 0.f;
       const int h = w.h[ti];
-      const bool live = q_row < w.len;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
-                            (static_cast<int64_t>(w.start + q_row) * a.Hq + h) * D;
+      const bool lva = qa < w.len, lvb = qb < w.len;
+      uint32_t* oa = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.o) +
+                                                 (static_cast<int64_t>(w.start + qa) * a.Hq + h) * D);
+      uint32_t* ob = oa + static_cast<int64_t>(8) * a.Hq * (D / 2);  // 8 rows further
+      const uint64_t ia2 = f2(inva, inva), ib2 = f2(invb, invb);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * c, o);
+        uint32_t o[16];
+        tmem_ld16x256_x4(tO + 32 * c, o);
         tmem_wait_ld();
-        if (live) {
-          const uint64_t inv2 = f2(inv, inv);
-          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float lo, hi;
-            unf2(fmul2(f2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2), lo, hi);
-            w[e] = pack_bf16(lo, hi);
-          }
-          // two 32-byte stores per 32 columns: whole sectors (rows are 256-B aligned)
-          st_global_v8(orow + 32 * c, w);
-          st_global_v8(orow + 32 * c + 16, w + 8);
+        for (int r = 0; r < 4; ++r) {
+          const int col2 = 16 * c + 4 * r + jq;  // bf16 pair index in the row
+          float x0, x1;
+          unf2(fmul2(f2(__uint_as_float(o[4 * r]), __uint_as_float(o[4 * r + 1])), ia2), x0, x1);
+          if (lva) oa[col2] = pack_bf16(x0, x1);
+          unf2(fmul2(f2(__uint_as_float(o[4 * r + 2]), __uint_as_float(o[4 * r + 3])), ib2), x0,
+               x1);
+          if (lvb) ob[col2] = pack_bf16(x0, x1);
         }
       }
-      if (a.lse && live)
-        a.lse[static_cast<int64_t>(h) * a.T + w.start + q_row] =
-            l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
+      if (a.lse && jq == 0) {
+        if (lva)
+          a.lse[static_cast<int64_t>(h) * a.T + w.start + qa] =
+              la > 0.f ? (ma + log2f(la)) * kLn2 : kNegInf;
+        if (lvb)
+          a.lse[static_cast<int64_t>(h) * a.T + w.start + qb] =
+              lb > 0.f ? (mb + log2f(lb)) * kLn2 : kNegInf;
+      }
       ++uc;
     }
     if (!ok && lane == 0) raise_err(a.err, kDevErrTimeout);
