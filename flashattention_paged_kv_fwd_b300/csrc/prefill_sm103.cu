@@ -103,7 +103,8 @@ struct PfCfg {
   static constexpr int B_OFULL = 10 + 2 * NSLOT;  // + query tile
   static constexpr int B_DRAIN = 12 + 2 * NSLOT;
   static constexpr int B_PVH0 = 13 + 2 * NSLOT;   // + query tile: PV over keys 0-63 done
-  static constexpr int NBAR = 15 + 2 * NSLOT;
+  static constexpr int B_EPI = 15 + 2 * NSLOT;    // + 4 * query tile + lane quarter
+  static constexpr int NBAR = 23 + 2 * NSLOT;
   static constexpr int OFF_SCHED = OFF_BAR + NBAR * 8 + 16;  // after the TMEM slot + abort flag
   static constexpr int SMEM = OFF_SCHED + 2 * kMaxSchedSeqs * 2 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -346,6 +347,7 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
         mbar_init(bar(C::B_PRDY + 2 * i + 1), kSoftmaxWarps / 2 * 32);
         mbar_init(bar(C::B_OFULL + i), 1);
         mbar_init(bar(C::B_PVH0 + i), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(C::B_EPI + 4 * i + q), 64);
       }
       for (int s = 0; s < C::NSLOT; ++s) {
         mbar_init(bar(C::B_FULL + s), 1);
@@ -796,34 +798,61 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap qmap,
       lb += __shfl_xor_sync(0xFFFFFFFFu, lb, 2);
       const float inva = la > 0.f ? 1.f / la : 0.f, invb = lb > 0.f ? 1.f / lb : 0.f;
       const int h = w.h[ti];
-      const bool lva = qa < w.len, lvb = qb < w.len;
-      uint32_t* oa = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.o) +
-                                                 (static_cast<int64_t>(w.start + qa) * a.Hq + h) * D);
-      uint32_t* ob = oa + static_cast<int64_t>(8) * a.Hq * (D / 2);  // 8 rows further
+      if (a.lse && jq == 0) {
+        if (qa < w.len)
+          a.lse[static_cast<int64_t>(h) * a.T + w.start + qa] =
+              la > 0.f ? (ma + log2f(la)) * kLn2 : kNegInf;
+        if (qb < w.len)
+          a.lse[static_cast<int64_t>(h) * a.T + w.start + qb] =
+              lb > 0.f ? (mb + log2f(lb)) * kLn2 : kNegInf;
+      }
+      // O / l in place for this warp's 16 rows ...
       const uint64_t ia2 = f2(inva, inva), ib2 = f2(invb, invb);
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[16];
         tmem_ld16x256_x4(tO + 32 * c, o);
         tmem_wait_ld();
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int col2 = 16 * c + 4 * r + jq;  // bf16 pair index in the row
           float x0, x1;
           unf2(fmul2(f2(__uint_as_float(o[4 * r]), __uint_as_float(o[4 * r + 1])), ia2), x0, x1);
-          if (lva) oa[col2] = pack_bf16(x0, x1);
+          o[4 * r] = __float_as_uint(x0);
+          o[4 * r + 1] = __float_as_uint(x1);
           unf2(fmul2(f2(__uint_as_float(o[4 * r + 2]), __uint_as_float(o[4 * r + 3])), ib2), x0,
                x1);
-          if (lvb) ob[col2] = pack_bf16(x0, x1);
+          o[4 * r + 2] = __float_as_uint(x0);
+          o[4 * r + 3] = __float_as_uint(x1);
         }
+        tmem_st16x256_x4(tO + 32 * c, o);
       }
-      if (a.lse && jq == 0) {
-        if (lva)
-          a.lse[static_cast<int64_t>(h) * a.T + w.start + qa] =
-              la > 0.f ? (ma + log2f(la)) * kLn2 : kNegInf;
-        if (lvb)
-          a.lse[static_cast<int64_t>(h) * a.T + w.start + qb] =
-              lb > 0.f ? (mb + log2f(lb)) * kLn2 : kNegInf;
+      tmem_wait_st();
+      // ... then, once the other warp of this lane quarter has done the same,
+      // this warp stores half of the columns of all 32 rows of the quarter:
+      // the 32x32b shape gives each thread one row's consecutive columns, so
+      // every store is a whole 32-byte sector
+      tc_fence_before();
+      mbar_arrive(bar(C::B_EPI + 4 * ti + q4));
+      if (!(ok = warp_wait(bar(C::B_EPI + 4 * ti + q4), uc & 1, abort_flag, a.wait_ns))) break;
+      tc_fence_after();
+      const int row = q0 + q4 * 32 + lane;  // query row within the sequence
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
+                            (static_cast<int64_t>(w.start + row) * a.Hq + h) * D + hh * (D / 2);
+      const uint32_t tq = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + C::TM_O +
+                          static_cast<uint32_t>(ti * D + hh * (D / 2));
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tq + 32 * c, o);
+        tmem_wait_ld();
+        if (row < w.len) {
+          uint32_t wv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            wv[e] = pack_bf16(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+          st_global_v8(orow + 32 * c, wv);
+          st_global_v8(orow + 32 * c + 16, wv + 8);
+        }
       }
       ++uc;
     }
