@@ -75,11 +75,7 @@ __device__ __forceinline__ SeqRange seq_range(int len, int max_blocks, int windo
 // accumulators (d/8 x 4 fp32) and Q fragments stay in registers.
 template <int D>
 constexpr int kMaxConsumerWarps = D == 128 ? 8 : 12;
-// Planner inputs: registers per thread of the two instantiations (ptxas -v,
-// rounded up to the allocation step) and shared memory per SM.
-constexpr int kRegsD128 = 168;
-constexpr int kRegsD64 = 120;
-constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kSmemPerSm = 228 * 1024;  // shared memory per SM (planner input)
 
 template <int D>
 __global__ void __launch_bounds__((kMaxConsumerWarps<D> + 1) * 32, 1)
@@ -492,6 +488,27 @@ void ensure_smem_attr(size_t bytes) {
   }
 }
 
+// Registers per thread of the bf16 decode kernel as compiled (read once per
+// device), rounded up to the allocation step of 8: the planner's count of
+// CTAs that fit on an SM follows the build instead of a number written down.
+int decode_regs(int d) {
+  static int cached[2][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int& c = cached[d == 128][dev];
+  if (!c) {
+    cudaFuncAttributes fa{};
+    const cudaError_t e = d == 128 ? cudaFuncGetAttributes(&fa, decode_bf16_kernel<128>)
+                                   : cudaFuncGetAttributes(&fa, decode_bf16_kernel<64>);
+    if (e != cudaSuccess || fa.numRegs <= 0) {
+      cudaGetLastError();
+      return 255;  // unknown: plan as if one CTA per SM
+    }
+    c = (fa.numRegs + 7) / 8 * 8;
+  }
+  return c;
+}
+
 }  // namespace
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_size, int window,
@@ -540,7 +557,7 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
     // holds most of an SM's shared memory and registers) runs in one wave
     // instead: the largest range count per sequence that still fits.
     if (!f32) {
-      const int regs = d == 128 ? kRegsD128 : kRegsD64;
+      const int regs = decode_regs(d);
       const int P = d / 64;
       const long long smem = 1024 + p.stages * (2LL * p.hg * P * kBox) + 64;
       long long cps = kSmemPerSm / (smem + 1024);

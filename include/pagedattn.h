@@ -343,7 +343,8 @@ PA_API int pa_attn_decode_paged(const void* q, const void* k_cache, const void* 
 /*
  * Workspace bytes attn_decode_paged needs for these arguments (0 when every
  * sequence fits one range). Host-only arithmetic except that num_splits = 0
- * reads the current device's SM count. Returns 0 on invalid arguments too.
+ * reads the current device's SM count and the decode kernel's register count
+ * (both cached per device). Returns 0 on invalid arguments too.
  */
 PA_API size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int max_blocks_per_seq,
                                  int block_size, int window, int num_splits);
