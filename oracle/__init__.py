@@ -19,6 +19,9 @@ Sources (web pages; cited by title and section):
 * "Cache KV, atención flash y optimización de la inferencia" (AI Engineering
   from Scratch, phase 07 lesson 12) -- standard vs tiled attention, the running
   (max, sum) softmax.
+* "Генерация и KV-кэш", sections "Сколько весит KV-кэш" and "Как уменьшить
+  кэш" -- a cache kept in FP8 (one byte per number); the format and its scale
+  are readings (E4M3, one scale per KV head).
 
 Every function is pinned by tests under ``tests/`` against values the pages
 print, closed forms, brute force or an independent library routine.
@@ -44,6 +47,15 @@ from .paged import (
     prefill_paged,
 )
 from .kv_bytes import kv_cache_bytes, kv_bytes_per_token_per_layer, mla_cache_bytes
+from .fp8 import (
+    E4M3_MAX,
+    e4m3_value,
+    e4m3_encode,
+    quantize_rows,
+    dequantize_pool,
+    append_paged_fp8,
+    decode_paged_fp8,
+)
 from .mla import (
     mla_absorb_query,
     mla_up_project,
@@ -53,6 +65,13 @@ from .mla import (
 )
 
 __all__ = [
+    "E4M3_MAX",
+    "e4m3_value",
+    "e4m3_encode",
+    "quantize_rows",
+    "dequantize_pool",
+    "append_paged_fp8",
+    "decode_paged_fp8",
     "attention_mask",
     "sdpa",
     "sdpa_rows",
