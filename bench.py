@@ -26,8 +26,10 @@ table walk) on a bounded sample of the same workload instead.
 same line with that family's metric: ``gqa_prefill_llama3_8b`` and
 ``chunked_prefill_llama3_8b`` (TFLOP/s), ``gqa_prefill_backward_llama3_8b``
 (TFLOP/s, 10*d FLOPs per visible pair and query head),
-``gqa_decode_llama3_70b``, ``mha_decode_gpt2`` and ``mla_decode_deepseek_v2``
-(GB/s of cache read), ``cow_copy_blocks_llama3_8b`` (GB/s read + written).
+``gqa_decode_llama3_70b``, ``mha_decode_gpt2``, ``gqa_decode_llama3_70b_fp8`` (an
+FP8 cache, one byte per number) and ``mla_decode_deepseek_v2`` (GB/s of cache
+read), ``cow_copy_blocks_llama3_8b`` (GB/s read + written). The default run also
+times each of them after the mixed step, under ``workloads``.
 """
 
 import argparse
@@ -65,7 +67,7 @@ def parse():
                     choices=["mixed_window4096", "gqa_decode_llama3_70b", "mha_decode_gpt2",
                              "gqa_prefill_llama3_8b", "chunked_prefill_llama3_8b",
                              "cow_copy_blocks_llama3_8b", "gqa_prefill_backward_llama3_8b",
-                             "mla_decode_deepseek_v2"],
+                             "mla_decode_deepseek_v2", "gqa_decode_llama3_70b_fp8"],
                     help="other workloads time a single kernel family (profiling aid)")
     ap.add_argument("--only", choices=["prefill", "append", "decode"], default=None,
                     help="run only one phase of the mixed step (profiling aid)")
@@ -87,7 +89,7 @@ def dist_info():
     return world, rank, local
 
 
-PHASES = ("prefill", "append", "decode", "copy", "backward", "mla")
+PHASES = ("prefill", "append", "decode", "copy", "backward", "mla", "decode_fp8")
 
 
 def max_over_ranks(phase_ms, step_ms, device):
@@ -125,6 +127,7 @@ KERNEL_SOURCES = {
     "prefill_backward": ("prefill_bwd.cu", "bwd_kernels.h", "pa_ptx.cuh", "capi_bwd.cu",
                          "host_util.h"),
     "mla_decode": ("mla_decode.cu", "mla_kernels.h", "pa_ptx.cuh", "capi_mla.cu", "host_util.h"),
+    "decode_fp8": ("decode_paged.cu", "pa_ptx.cuh", "pa_kernels.h", "capi.cu", "host_util.h"),
 }
 
 
@@ -375,6 +378,20 @@ class SingleStep:
             self.dbytes = float(sum(w["lengths"])) * 576 * 2
             self.phase = "mla"
             self.launches = {"mla": 2 if need > 0 else 1}
+        elif name == "gqa_decode_llama3_70b_fp8":
+            # the Llama-3-70B decode over an FP8 (E4M3) cache: one byte per
+            # cached number, per-KV-head scales
+            w = inputs.gqa_decode_llama3_70b_fp8(device, batch=decode_batch)
+            self.w = w
+            self.out = torch.empty_like(w["q"])
+            self.lse = torch.empty((w["hq"], w["q"].shape[0]), dtype=torch.float32, device=device)
+            need = binding.decode_workspace_bytes(w["q"].shape[0], w["hq"], w["hkv"], w["d"],
+                                                  w["block_table"].shape[1], 16, 0)
+            self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+            self.flops = 0.0
+            self.dbytes = decode_bytes(w["lengths"], w["hkv"], w["d"], 0, elem=1)
+            self.phase = "decode_fp8"
+            self.launches = {"decode_fp8": 2 if need > 0 else 1}
         elif name == "gqa_prefill_llama3_8b":
             w = inputs.gqa_prefill_llama3_8b(device)
             self.w = w
@@ -408,6 +425,11 @@ class SingleStep:
             self.b.mla_decode_paged(w["q"], w["cache"], w["block_table"], w["seq_lens"],
                                     scale=w["scale"], out=self.out, lse=self.lse,
                                     workspace=self.ws, err_flag=self.err)
+        elif self.phase == "decode_fp8":
+            self.b.attn_decode_paged_fp8(w["q"], w["k_cache"], w["v_cache"], w["k_scale"],
+                                         w["v_scale"], w["block_table"], w["seq_lens"],
+                                         out=self.out, lse=self.lse, workspace=self.ws,
+                                         err_flag=self.err)
         elif self.phase == "backward":
             self.b.attn_prefill_backward(w["q"], w["k"], w["v"], self.out, self.dout, self.lse,
                                          causal=True, cu_seqlens=w["cu_seqlens"],
@@ -563,10 +585,12 @@ def time_steps(run_phase, phases, n, flush, stream):
 # chunked prefill, backward, MLA decode and copy-on-write workloads
 EXTRA_WORKLOADS = ("mha_decode_gpt2", "gqa_prefill_llama3_8b", "gqa_decode_llama3_70b",
                    "chunked_prefill_llama3_8b", "gqa_prefill_backward_llama3_8b",
-                   "mla_decode_deepseek_v2", "cow_copy_blocks_llama3_8b")
+                   "mla_decode_deepseek_v2", "cow_copy_blocks_llama3_8b",
+                   "gqa_decode_llama3_70b_fp8")
 
 PHASE_KERNEL = {"prefill": "prefill_bf16", "append": "kv_append", "decode": "decode_bf16",
-                "copy": "copy_blocks", "backward": "prefill_backward", "mla": "mla_decode"}
+                "copy": "copy_blocks", "backward": "prefill_backward", "mla": "mla_decode",
+                "decode_fp8": "decode_fp8"}
 
 
 def phase_rate(phase, work, ms, world):
@@ -578,7 +602,8 @@ def phase_rate(phase, work, ms, world):
 
 def phase_work(st, phase):
     return {"prefill": st.flops, "backward": st.flops, "decode": st.dbytes, "mla": st.dbytes,
-            "copy": getattr(st, "cbytes", 0.0), "append": getattr(st, "abytes", 0.0)}[phase]
+            "decode_fp8": st.dbytes, "copy": getattr(st, "cbytes", 0.0),
+            "append": getattr(st, "abytes", 0.0)}[phase]
 
 
 def roofline_of(phase, achieved, peaks, peak_src, workload):
@@ -773,6 +798,7 @@ def run_ours(args):
         {"prefill": "causal prefill attention TFLOP/s", "decode": "paged decode KV-read GB/s",
          "backward": "causal prefill attention backward TFLOP/s (10*d per visible pair)",
          "mla": "MLA decode latent-read GB/s",
+         "decode_fp8": "paged decode FP8-cache-read GB/s",
          "copy": "copy-on-write block copy GB/s (read + written)"}[head],
         "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,

@@ -454,6 +454,93 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, *, window=0, s
     return out, lse
 
 
+def _fp8_fns():
+    lib = load_library()
+    if not getattr(lib, "_fp8_typed", False):
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.pa_kv_append_paged_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32,
+                                               i32, i32, i32, i32, vp, vp]
+        lib.pa_kv_append_paged_fp8.restype = i32
+        lib.pa_attn_decode_paged_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, i32,
+                                                 i32, i32, i32, i32, i32, i32, f32, i32, vp, sz,
+                                                 vp, vp]
+        lib.pa_attn_decode_paged_fp8.restype = i32
+        lib._fp8_typed = True
+    return lib
+
+
+def kv_append_paged_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                        *, cu_new=None, err_flag=None, stream=None):
+    """Quantise new bf16 K/V rows [T_new, Hkv, d] with the heads' scales
+    (float32 [Hkv]) and write the E4M3 codes into the uint8 pools
+    [num_blocks, block_size, Hkv, d] in place (seq_lens: lengths BEFORE the
+    append; cu_new int32 [B+1] or None for one token per sequence)."""
+    lib = _fp8_fns()
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _cuda_contig(name, t, torch.bfloat16)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda_contig(name, t, torch.uint8)
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _cuda_contig(name, t, torch.float32)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("seq_lens", seq_lens, torch.int32)
+    num_blocks, block_size, hkv, d = k_cache.shape
+    _need(v_cache.shape == k_cache.shape, "k_cache and v_cache differ in shape")
+    _need(k_new.dim() == 3 and k_new.shape[1:] == (hkv, d) and v_new.shape == k_new.shape,
+          "k_new/v_new must be [T_new, Hkv, d]")
+    _need(k_scale.numel() == hkv and v_scale.numel() == hkv, "scales must have Hkv entries")
+    B = seq_lens.numel()
+    _need(block_table.dim() == 2 and block_table.shape[0] == B, "block_table must be [B, max_blocks]")
+    if cu_new is not None:
+        _cuda_contig("cu_new", cu_new, torch.int32)
+        _need(cu_new.numel() == B + 1, "cu_new must have B+1 entries")
+    st = lib.pa_kv_append_paged_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+                                    block_table.shape[1], _ptr(seq_lens), _ptr(cu_new),
+                                    k_new.shape[0], B, hkv, d, block_size, num_blocks,
+                                    _ptr(err_flag), _stream(stream))
+    _check(st, "kv_append_paged_fp8")
+
+
+def attn_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, *,
+                          window=0, scale=None, num_splits=0, out=None, lse=None,
+                          return_lse=True, workspace=None, err_flag=None, stream=None):
+    """attn_decode_paged over FP8 pools: q bf16 [B, Hq, d]; pools uint8
+    [num_blocks, 16, Hkv, d] of E4M3 codes; k_scale, v_scale float32 [Hkv].
+    Returns (o bf16 [B, Hq, d], lse float32 [Hq, B])."""
+    lib = _fp8_fns()
+    _cuda_contig("q", q, torch.bfloat16)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _cuda_contig(name, t, torch.uint8)
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _cuda_contig(name, t, torch.float32)
+    _cuda_contig("block_table", block_table, torch.int32)
+    _cuda_contig("seq_lens", seq_lens, torch.int32)
+    B, hq, d = q.shape
+    num_blocks, block_size, hkv, dk = k_cache.shape
+    _need(dk == d and v_cache.shape == k_cache.shape, "pool shapes do not match q")
+    _need(k_scale.numel() == hkv and v_scale.numel() == hkv, "scales must have Hkv entries")
+    _need(block_table.dim() == 2 and block_table.shape[0] == B, "block_table must be [B, max_blocks]")
+    _need(seq_lens.numel() == B, "seq_lens must have B entries")
+    max_blocks = block_table.shape[1]
+    need = decode_workspace_bytes(B, hq, hkv, d, max_blocks, block_size, window, num_splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((hq, B), dtype=torch.float32, device=q.device)
+    st = lib.pa_attn_decode_paged_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                      _ptr(v_scale), _ptr(block_table), max_blocks,
+                                      _ptr(seq_lens), _ptr(out), _ptr(lse), B, hq, hkv, d,
+                                      block_size, num_blocks, int(window or 0),
+                                      float(scale or 0.0), int(num_splits), _ptr(workspace),
+                                      0 if workspace is None else workspace.numel(),
+                                      _ptr(err_flag), _stream(stream))
+    _check(st, "attn_decode_paged_fp8")
+    return out, lse
+
+
 def default_scale(head_dim):
     return 1.0 / math.sqrt(head_dim)
 

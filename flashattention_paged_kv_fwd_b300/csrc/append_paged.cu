@@ -100,7 +100,91 @@ kv_append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_ne
   }
 }
 
+// FP8 cache: each new bf16 row is quantised on the way in. Element e of the
+// row belongs to KV head e / d; y = x / scale[head] with IEEE division, then
+// the nearest E4M3 code (ties to even, saturating to +-448). One warp per
+// token; a lane handles 8 elements (16 bytes in, 8 bytes out) at a time.
+__global__ void __launch_bounds__(kAppendWarps * 32)
+kv_append_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                     uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
+                     const float* __restrict__ k_scale, const float* __restrict__ v_scale,
+                     const int32_t* __restrict__ table, int max_blocks,
+                     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_new,
+                     int n_seq, int n_tok, int row_vecs, int d, int block_size, int num_blocks,
+                     int32_t* err) {
+  __shared__ int32_t cu_s[kMaxCuInSmem + 1];
+  const bool staged = cu_new != nullptr && n_seq <= kMaxCuInSmem;
+  if (staged) {
+    for (int i = threadIdx.x; i <= n_seq; i += blockDim.x) cu_s[i] = cu_new[i];
+    __syncthreads();
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kAppendWarps + warp;
+  if (t >= n_tok) return;
+  int b, first;
+  if (cu_new == nullptr) {
+    b = t;
+    first = t;
+  } else {
+    const int32_t* cu = staged ? cu_s : cu_new;
+    if (t < cu[0] || t >= cu[n_seq]) {
+      if (lane == 0) raise_err(err, kDevErrBadPosition);
+      return;
+    }
+    b = find_sequence(cu, n_seq, t);
+    first = cu[b];
+  }
+  const int pos = seq_lens[b] + (t - first);
+  const int lblk = pos / block_size;
+  if (pos < 0 || lblk >= max_blocks) {
+    if (lane == 0) raise_err(err, kDevErrBadPosition);
+    return;
+  }
+  const int blk = table[static_cast<int64_t>(b) * max_blocks + lblk];
+  if (blk < 0 || blk >= num_blocks) {
+    if (lane == 0) raise_err(err, kDevErrBadBlock);
+    return;
+  }
+  const int64_t src = static_cast<int64_t>(t) * row_vecs;
+  const int64_t dst = (static_cast<int64_t>(blk) * block_size + pos % block_size) * row_vecs;
+  auto quant = [&](const uint4& x, float sc) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float y0 = __fdiv_rn(__uint_as_float(w[2 * e] << 16), sc);
+      const float y1 = __fdiv_rn(__uint_as_float(w[2 * e] & 0xFFFF0000u), sc);
+      const float y2 = __fdiv_rn(__uint_as_float(w[2 * e + 1] << 16), sc);
+      const float y3 = __fdiv_rn(__uint_as_float(w[2 * e + 1] & 0xFFFF0000u), sc);
+      out[e] = static_cast<uint32_t>(f32x2_to_e4m3x2(y0, y1)) |
+               (static_cast<uint32_t>(f32x2_to_e4m3x2(y2, y3)) << 16);
+    }
+    return make_uint2(out[0], out[1]);
+  };
+  for (int i = lane; i < row_vecs; i += 32) {
+    const int head = (i * 8) / d;
+    const uint4 kx = __ldg(k_new + src + i);
+    const uint4 vx = __ldg(v_new + src + i);
+    k_cache[dst + i] = quant(kx, k_scale[head]);
+    v_cache[dst + i] = quant(vx, v_scale[head]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                 void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* table, int max_blocks, const int32_t* seq_lens,
+                                 const int32_t* cu_new, int n_tok, int n_seq, int Hkv, int d,
+                                 int block_size, int num_blocks, int32_t* err, cudaStream_t s) {
+  if (n_tok == 0) return cudaSuccess;
+  const int grid = (n_tok + kAppendWarps - 1) / kAppendWarps;
+  kv_append_fp8_kernel<<<grid, kAppendWarps * 32, 0, s>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+      static_cast<uint2*>(k_cache), static_cast<uint2*>(v_cache), k_scale, v_scale, table,
+      max_blocks, seq_lens, cu_new, n_seq, n_tok, Hkv * d / 8, d, block_size, num_blocks, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_kv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                              const int32_t* table, int max_blocks, const int32_t* seq_lens,

@@ -183,7 +183,11 @@ size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int max_blocks_p
                                            num_splits, num_splits > 0 ? 0 : sm_count(), false);
   const pa::DecodePlan pf = pa::plan_decode(B, Hq, Hkv, d, max_blocks_per_seq, block_size, window,
                                             num_splits, num_splits > 0 ? 0 : sm_count(), true);
-  return p.workspace > pf.workspace ? p.workspace : pf.workspace;
+  const pa::DecodePlan p8 = pa::plan_decode(B, Hq, Hkv, d, max_blocks_per_seq, block_size, window,
+                                            num_splits, num_splits > 0 ? 0 : sm_count(), false,
+                                            true);
+  size_t w = p.workspace > pf.workspace ? p.workspace : pf.workspace;
+  return w > p8.workspace ? w : p8.workspace;
 }
 
 int pa_attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
@@ -239,6 +243,81 @@ int pa_attn_decode_paged(const void* q, const void* k_cache, const void* v_cache
       return PA_ERR_CUDA;
     e = pa::launch_decode_bf16(a, p, km, vm, s);
   }
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_kv_append_paged_fp8(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                           const float* k_scale, const float* v_scale, const int32_t* block_table,
+                           int max_blocks_per_seq, const int32_t* seq_lens, const int32_t* cu_new,
+                           int num_new_tokens, int B, int Hkv, int d, int block_size,
+                           int num_blocks, int32_t* err_flag, void* stream) {
+  if (B <= 0 || Hkv <= 0 || num_new_tokens < 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
+      block_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PA_ERR_INVALID_ARG;
+  if (!k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale || !block_table ||
+      !seq_lens)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 8) || !aligned(v_cache, 8) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4) || (cu_new && !aligned(cu_new, 4)) ||
+      (err_flag && !aligned(err_flag, 4)))
+    return PA_ERR_INVALID_ARG;
+  if (!cu_new && num_new_tokens != B) return PA_ERR_INVALID_ARG;
+  const cudaError_t e = pa::launch_kv_append_fp8(
+      k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table, max_blocks_per_seq, seq_lens,
+      cu_new, num_new_tokens, B, Hkv, d, block_size, num_blocks, err_flag,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_attn_decode_paged_fp8(const void* q, const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale,
+                             const int32_t* block_table, int max_blocks_per_seq,
+                             const int32_t* seq_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                             int d, int block_size, int num_blocks, int window, float scale,
+                             int num_splits, void* workspace, size_t workspace_bytes,
+                             int32_t* err_flag, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0 || num_splits < 0)
+    return PA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PA_ERR_INVALID_ARG;
+  if (block_size != 16) return PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
+    return PA_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !o)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(block_table, 4) ||
+      !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (err_flag && !aligned(err_flag, 4)))
+    return PA_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
+  if ((Hq / Hkv + 15) / 16 > (d == 128 ? 8 : 12)) return PA_ERR_UNSUPPORTED;
+  const pa::DecodePlan p = pa::plan_decode(B, Hq, Hkv, d, max_blocks_per_seq, block_size, window,
+                                           num_splits, num_splits > 0 ? 0 : sm_count(), false,
+                                           true);
+  if (p.smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
+  if (p.workspace > 0 && (!workspace || workspace_bytes < p.workspace)) return PA_ERR_WORKSPACE;
+
+  pa::DecodeArgs a{};
+  a.q = q; a.o = o; a.lse = lse; a.k_cache = k_cache; a.v_cache = v_cache;
+  a.table = block_table; a.seq_lens = seq_lens; a.err = err_flag;
+  if (p.workspace > 0) {
+    const size_t n = static_cast<size_t>(B) * Hq * p.num_splits;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        (n * d * 4 + 255) / 256 * 256);
+  }
+  a.max_blocks = max_blocks_per_seq; a.num_blocks = num_blocks; a.B = B; a.Hq = Hq;
+  a.Hkv = Hkv; a.d = d; a.window = window > 0 ? window : 0;
+  a.scale_log2 = scale_log2(scale, d);
+  a.wait_ns = pa::role_wait_limit_ns();
+  CUtensorMap km, vm;
+  if (!encode_pool_u8(&km, k_cache, d, Hkv, block_size, num_blocks, p.hg) ||
+      !encode_pool_u8(&vm, v_cache, d, Hkv, block_size, num_blocks, p.hg))
+    return PA_ERR_CUDA;
+  const cudaError_t e = pa::launch_decode_fp8(a, p, km, vm, k_scale, v_scale,
+                                              static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

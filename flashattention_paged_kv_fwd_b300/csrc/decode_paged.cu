@@ -77,6 +77,102 @@ template <int D>
 constexpr int kMaxConsumerWarps = D == 128 ? 8 : 12;
 constexpr int kSmemPerSm = 228 * 1024;  // shared memory per SM (planner input)
 
+// One page (16 tokens) of one KV head for the 16 query-head rows of a
+// consumer warp: S = Q K^T on the tensor cores, the mask of tokens outside
+// [first visible, seq_len), the online softmax update (log2 domain) and
+// O += P V. kb / vb: the page's K / V tile of this head in shared memory
+// (64-column panel p at + p * hg * kBox), 128-byte swizzled. F16: the tiles,
+// the query fragments and P are fp16 (the FP8 cache's path), else bf16.
+template <int D, bool F16>
+__device__ __forceinline__ void consume_page(const uint32_t (&qa)[D / 16][4], uint32_t kb,
+                                             uint32_t vb, int hg, int tok0, const SeqRange& r,
+                                             float sl2, int mi, int tq, int ktok, int vtok,
+                                             float& m0, float& m1, float& l0, float& l1,
+                                             float (&acc)[D / 8][4]) {
+  auto mma = [](float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (F16)
+      mma_f16_16816(c, a, b0, b1);
+    else
+      mma_bf16_16816(c, a, b0, b1);
+  };
+  float sc[2][4];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const int c = kk * 2 + (mi & 1);
+    const uint32_t addr = kb + (c >> 3) * hg * kBox + ktok * 128 + (((c & 7) ^ (ktok & 7)) << 4);
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4(addr, b0, b1, b2, b3);
+    mma(sc[0], qa[kk], b0, b1);
+    mma(sc[1], qa[kk], b2, b3);
+  }
+
+  const bool edge = (tok0 + kBlk > r.len) || (tok0 < r.t_begin);
+  uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+  if (edge) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = tok0 + 8 * t + 2 * tq + (e & 1);
+        if (tok >= r.len || tok < r.t_begin) sc[t][e] = kNegInf;
+      }
+    auto ok = [&](int tok) { return tok < r.len && tok >= r.t_begin; };
+    const int ta = tok0 + 2 * tq, tb = tok0 + 8 + 2 * tq;
+    mlo = (ok(ta) ? 0x0000FFFFu : 0u) | (ok(ta + 1) ? 0xFFFF0000u : 0u);
+    mhi = (ok(tb) ? 0x0000FFFFu : 0u) | (ok(tb + 1) ? 0xFFFF0000u : 0u);
+  }
+
+  // online softmax (log2 domain), rows gr (e = 0,1) and gr + 8 (e = 2,3)
+  float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) * sl2;
+  float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])) * sl2;
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+  const float mu0 = mn0 == kNegInf ? 0.f : mn0;
+  const float mu1 = mn1 == kNegInf ? 0.f : mn1;
+  const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+  m0 = mn0;
+  m1 = mn1;
+  float ps[2][4];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    ps[t][0] = ex2(fmaf(sc[t][0], sl2, -mu0));
+    ps[t][1] = ex2(fmaf(sc[t][1], sl2, -mu0));
+    ps[t][2] = ex2(fmaf(sc[t][2], sl2, -mu1));
+    ps[t][3] = ex2(fmaf(sc[t][3], sl2, -mu1));
+  }
+  l0 = l0 * al0 + (ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1]);
+  l1 = l1 * al1 + (ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3]);
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j) {
+    acc[j][0] *= al0;
+    acc[j][1] *= al0;
+    acc[j][2] *= al1;
+    acc[j][3] *= al1;
+  }
+  auto pack = [](float lo, float hi) {
+    if constexpr (F16)
+      return pack_f16(lo, hi);
+    else
+      return pack_bf16(lo, hi);
+  };
+  const uint32_t pa[4] = {pack(ps[0][0], ps[0][1]), pack(ps[0][2], ps[0][3]),
+                          pack(ps[1][0], ps[1][1]), pack(ps[1][2], ps[1][3])};
+#pragma unroll
+  for (int jj = 0; jj < D / 16; ++jj) {
+    const int c = jj * 2 + (mi >> 1);
+    const uint32_t addr = vb + (c >> 3) * hg * kBox + vtok * 128 + (((c & 7) ^ (vtok & 7)) << 4);
+    uint32_t v0, v1, v2, v3;
+    ldsm_x4_t(addr, v0, v1, v2, v3);
+    mma(acc[2 * jj], pa, v0 & mlo, v1 & mhi);
+    mma(acc[2 * jj + 1], pa, v2 & mlo, v3 & mhi);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__((kMaxConsumerWarps<D> + 1) * 32, 1)
 decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -215,82 +311,10 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
       break;
     }
     const int phys = phys_s[st];
-    if (phys >= 0) {
-      const uint32_t kb = base + st * stage_bytes + g * kBox;           // panel p at + p*hg*kBox
-      const uint32_t vb = base + st * stage_bytes + (P * hg + g) * kBox;
-      const int tok0 = (pstart + i) * kBlk;
-
-      float sc[2][4];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int c = kk * 2 + (mi & 1);
-        const uint32_t addr = kb + (c >> 3) * hg * kBox + ktok * 128 + (((c & 7) ^ (ktok & 7)) << 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(addr, b0, b1, b2, b3);
-        mma_bf16_16816(sc[0], qa[kk], b0, b1);
-        mma_bf16_16816(sc[1], qa[kk], b2, b3);
-      }
-
-      const bool edge = (tok0 + kBlk > r.len) || (tok0 < r.t_begin);
-      uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
-      if (edge) {
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = tok0 + 8 * t + 2 * tq + (e & 1);
-            if (tok >= r.len || tok < r.t_begin) sc[t][e] = kNegInf;
-          }
-        auto ok = [&](int tok) { return tok < r.len && tok >= r.t_begin; };
-        const int ta = tok0 + 2 * tq, tb = tok0 + 8 + 2 * tq;
-        mlo = (ok(ta) ? 0x0000FFFFu : 0u) | (ok(ta + 1) ? 0xFFFF0000u : 0u);
-        mhi = (ok(tb) ? 0x0000FFFFu : 0u) | (ok(tb + 1) ? 0xFFFF0000u : 0u);
-      }
-
-      // online softmax (log2 domain), rows gr (e = 0,1) and gr + 8 (e = 2,3)
-      float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) * sl2;
-      float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])) * sl2;
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float mu0 = mn0 == kNegInf ? 0.f : mn0;
-      const float mu1 = mn1 == kNegInf ? 0.f : mn1;
-      const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
-      m0 = mn0;
-      m1 = mn1;
-      float ps[2][4];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        ps[t][0] = ex2(fmaf(sc[t][0], sl2, -mu0));
-        ps[t][1] = ex2(fmaf(sc[t][1], sl2, -mu0));
-        ps[t][2] = ex2(fmaf(sc[t][2], sl2, -mu1));
-        ps[t][3] = ex2(fmaf(sc[t][3], sl2, -mu1));
-      }
-      l0 = l0 * al0 + (ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1]);
-      l1 = l1 * al1 + (ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3]);
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        acc[j][0] *= al0;
-        acc[j][1] *= al0;
-        acc[j][2] *= al1;
-        acc[j][3] *= al1;
-      }
-      const uint32_t pa[4] = {pack_bf16(ps[0][0], ps[0][1]), pack_bf16(ps[0][2], ps[0][3]),
-                              pack_bf16(ps[1][0], ps[1][1]), pack_bf16(ps[1][2], ps[1][3])};
-#pragma unroll
-      for (int jj = 0; jj < D / 16; ++jj) {
-        const int c = jj * 2 + (mi >> 1);
-        const uint32_t addr = vb + (c >> 3) * hg * kBox + vtok * 128 + (((c & 7) ^ (vtok & 7)) << 4);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(addr, v0, v1, v2, v3);
-        mma_bf16_16816(acc[2 * jj], pa, v0 & mlo, v1 & mhi);
-        mma_bf16_16816(acc[2 * jj + 1], pa, v2 & mlo, v3 & mhi);
-      }
-    }
+    if (phys >= 0)
+      consume_page<D, false>(qa, base + st * stage_bytes + g * kBox,
+                             base + st * stage_bytes + (P * hg + g) * kBox, hg,
+                             (pstart + i) * kBlk, r, sl2, mi, tq, ktok, vtok, m0, m1, l0, l1, acc);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty(st));
   }
@@ -308,6 +332,233 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
     const float l = half ? l1 : l0;
     const float m = half ? m1 : m0;
     const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
+    const int64_t bh = static_cast<int64_t>(b) * a.Hq + h;
+    if (single) {
+      uint32_t* o32 = static_cast<uint32_t*>(a.o) + bh * (D / 2);
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j)
+        o32[j * 4 + tq] = pack_bf16(acc[j][2 * half] * inv, acc[j][2 * half + 1] * inv);
+      if (tq == 0 && a.lse) a.lse[h * a.B + b] = lse_v;
+    } else {
+      float2* w = reinterpret_cast<float2*>(a.ws_o + (bh * num_splits + s) * D);
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j)
+        w[j * 4 + tq] = make_float2(acc[j][2 * half] * inv, acc[j][2 * half + 1] * inv);
+      if (tq == 0) a.ws_lse[bh * num_splits + s] = lse_v;
+    }
+  }
+}
+
+// ------------------------------------------------------- FP8 (E4M3) cache path
+// The same decode over pools of E4M3 codes with one fp32 scale per KV head for
+// keys and one for values (a code q stands for value(q) * scale). A page's
+// codes arrive by TMA (one box of 16 tokens x hg heads x d bytes for K and one
+// for V: half the bytes of the bf16 path). Each consumer warp converts its own
+// head's K and V tiles to fp16 -- every E4M3 value is an fp16 value, one
+// conversion per pair -- into a private tile in the swizzled layout of the bf16
+// path, releases the stage, and runs the same page update with fp16 warp MMAs
+// (the query is rounded to fp16 once, exactly for bf16 values of magnitude
+// 2^-14 .. 65504). The key scale is folded into the softmax scale of the
+// head and the value scale into its output, so no element is rescaled.
+template <int D>
+__global__ void __launch_bounds__((kMaxConsumerWarps<D> + 1) * 32, 1)
+decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap vmap, const DecodeArgs a,
+                  const float* __restrict__ k_scale, const float* __restrict__ v_scale,
+                  const int chunk, const int num_splits, const int hg, const int mt,
+                  const int ns) {
+  constexpr int P = D / 64;
+  const int G = a.Hq / a.Hkv;
+  const int b = blockIdx.z, hc = blockIdx.y, s = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = hg * mt;  // consumer warps
+
+  const SeqRange r = seq_range(a.seq_lens[b], a.max_blocks, a.window, chunk, a.err,
+                               s == 0 && hc == 0 && threadIdx.x == 0);
+  if (s >= (r.n_split > 0 ? r.n_split : 1)) return;
+
+  if (r.n_pages == 0) {  // no visible key: o = 0, lse = -inf
+    const int h0 = hc * hg * G, nh = hg * G;
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.o);
+    for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
+      o[(static_cast<int64_t>(b) * a.Hq + h0) * D + i] = __float2bfloat16_rn(0.f);
+    if (a.lse)
+      for (int i = threadIdx.x; i < nh; i += blockDim.x) a.lse[(h0 + i) * a.B + b] = kNegInf;
+    return;
+  }
+  const int pstart = r.p_begin + s * chunk;
+  const int npg = min(chunk, r.n_pages - s * chunk);
+  const bool single = r.n_split == 1;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t stage_bytes = 2u * hg * kBlk * D;  // K codes [hg][16][D], then V codes
+  const uint32_t bars = base + ns * stage_bytes;  // full[ns], empty[ns]
+  int32_t* phys_s = reinterpret_cast<int32_t*>(gbase + ns * stage_bytes + 16 * ns);
+  int32_t* tab_s = phys_s + ns;
+  volatile int32_t* abort_s = tab_s + chunk;
+  // per-warp fp16 tiles: K panels then V panels, 16 tokens x 128 bytes each
+  const uint32_t stg0 =
+      (smem_u32(const_cast<const int32_t*>(abort_s) + 1) + 1023u) & ~1023u;
+  auto full = [&](int i) { return bars + 8u * i; };
+  auto empty = [&](int i) { return bars + 8u * (ns + i); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), nw);
+    }
+    *abort_s = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < npg; i += blockDim.x)
+    tab_s[i] = a.table[static_cast<int64_t>(b) * a.max_blocks + pstart + i];
+  __syncthreads();
+
+  if (warp == nw) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+      int issued = 0;
+      uint32_t valid_mask = 0;  // validity of the last `ns` issued blocks (bit per stage)
+      for (int i = 0; i < npg; ++i) {
+        const int st = i % ns, u = i / ns;
+        if (u > 0 && !mbar_wait(empty(st), (u - 1) & 1, a.wait_ns)) {
+          raise_err(a.err, kDevErrTimeout);
+          *abort_s = 1;
+          break;
+        }
+        if (*abort_s) break;
+        const int phys = tab_s[i];
+        const bool ok = phys >= 0 && phys < a.num_blocks;
+        if (!ok) raise_err(a.err, kDevErrBadBlock);
+        phys_s[st] = ok ? phys : -1;
+        if (ok) {
+          mbar_arrive_expect_tx(full(st), stage_bytes);
+          const uint32_t sb = base + st * stage_bytes;
+          tma_load_4d(sb, &kmap, full(st), 0, 0, hc * hg, phys);
+          tma_load_4d(sb + stage_bytes / 2, &vmap, full(st), 0, 0, hc * hg, phys);
+          valid_mask |= 1u << st;
+        } else {
+          valid_mask &= ~(1u << st);
+          mbar_arrive(full(st));
+        }
+        issued = i + 1;
+      }
+      for (int i = issued - ns > 0 ? issued - ns : 0; i < issued; ++i) {
+        const int st = i % ns;
+        if (valid_mask & (1u << st)) mbar_wait(full(st), (i / ns) & 1, 100000000ull);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = warp / mt, mti = warp % mt;
+  const int kvh = hc * hg + g;
+  const int qh0 = kvh * G + mti * 16;
+  const int nrows = min(16, G - mti * 16);
+  const int gr = lane >> 2, tq = lane & 3;
+  const float sl2 = a.scale_log2 * k_scale[kvh];
+  const float vsc = v_scale[kvh];
+  const uint32_t stg_k = stg0 + static_cast<uint32_t>(warp * 2 * P * kBox);
+  const uint32_t stg_v = stg_k + P * kBox;
+
+  // query fragments, rounded to fp16
+  uint32_t qa[D / 16][4];
+  {
+    const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
+    const int64_t ra = (static_cast<int64_t>(b) * a.Hq + qh0 + gr) * (D / 2);
+    const int64_t rb = ra + 8 * (D / 2);
+    auto h2 = [](uint32_t w) {
+      return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    };
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = gr < nrows ? h2(q32[ra + kk * 8 + tq]) : 0u;
+      qa[kk][1] = gr + 8 < nrows ? h2(q32[rb + kk * 8 + tq]) : 0u;
+      qa[kk][2] = gr < nrows ? h2(q32[ra + kk * 8 + 4 + tq]) : 0u;
+      qa[kk][3] = gr + 8 < nrows ? h2(q32[rb + kk * 8 + 4 + tq]) : 0u;
+    }
+  }
+
+  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
+  float acc[D / 8][4];
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+  const int mi = lane >> 3, rr = lane & 7;
+  const int ktok = ((mi >> 1) << 3) + rr;
+  const int vtok = ((mi & 1) << 3) + rr;
+
+  for (int i = 0; i < npg; ++i) {
+    const int st = i % ns;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(full(st), (i / ns) & 1, a.wait_ns))) {
+      if (lane == 0) raise_err(a.err, kDevErrTimeout);
+      *abort_s = 1;
+      break;
+    }
+    const int phys = phys_s[st];
+    if (phys >= 0) {
+      // lane i takes bytes [512 j + 16 i, +16) of the head's 16 x D tile of
+      // codes: consecutive lanes read consecutive 16-byte pieces (no bank
+      // conflicts), each covering 16 elements of one token row
+      const uint8_t* tile = gbase + st * stage_bytes + static_cast<uint32_t>(g * kBlk * D);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint8_t* src = tile + t * (stage_bytes / 2);
+        const uint32_t dst = t ? stg_v : stg_k;
+#pragma unroll
+        for (int j = 0; j < kBlk * D / 512; ++j) {
+          const int off = 512 * j + 16 * lane;
+          const int row = off / D, e0 = off % D;
+          const uint4 w = *reinterpret_cast<const uint4*>(src + off);
+          const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            h[2 * e] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws4[e] & 0xFFFFu));
+            h[2 * e + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws4[e] >> 16));
+          }
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int el = e0 + 8 * half;
+            const int p = el >> 6, c = (el & 63) >> 3;
+            const uint32_t addr =
+                dst + p * kBox + row * 128 + ((static_cast<uint32_t>(c) ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                         "r"(h[4 * half]), "r"(h[4 * half + 1]), "r"(h[4 * half + 2]),
+                         "r"(h[4 * half + 3])
+                         : "memory");
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(st));  // the codes are converted: the stage is free
+    if (phys >= 0)
+      consume_page<D, true>(qa, stg_k, stg_v, 1, (pstart + i) * kBlk, r, sl2, mi, tq, ktok, vtok,
+                            m0, m1, l0, l1, acc);
+    __syncwarp();  // every lane is done with the private tiles before the next page
+  }
+
+  // ------------------------------------------------------------- epilogue
+  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int row = gr + 8 * half;
+    if (row >= nrows) continue;
+    const int h = qh0 + row;
+    const float l = half ? l1 : l0;
+    const float m = half ? m1 : m0;
+    const float inv = l > 0.f ? vsc / l : 0.f;
     const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
     const int64_t bh = static_cast<int64_t>(b) * a.Hq + h;
     if (single) {
@@ -509,10 +760,24 @@ int decode_regs(int d) {
   return c;
 }
 
+int g_attr8_done[2][64];
+
+template <int D>
+void ensure_smem_attr_fp8(size_t bytes) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (g_attr8_done[D == 128][dev] < static_cast<int>(bytes)) {
+    cudaFuncSetAttribute(decode_fp8_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(bytes));
+    g_attr8_done[D == 128][dev] = static_cast<int>(bytes);
+  }
+}
+
 }  // namespace
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_size, int window,
-                       int num_splits_req, int sm_count, bool f32) {
+                       int num_splits_req, int sm_count, bool f32, bool fp8) {
   DecodePlan p{};
   const int G = Hq / Hkv;
   const int sms = sm_count > 0 ? sm_count : 148;
@@ -537,8 +802,11 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
       if (Hkv % c == 0 && c * p.mt <= max_warps && 2 * c * P * kBox <= 64 * 1024) hg = c;
     p.hg = hg;
     p.head_chunks = Hkv / hg;
-    const int stage = 2 * hg * P * kBox;
-    int ns = (200 * 1024) / stage;
+    // FP8 pages are half the bytes; each consumer warp also keeps a private
+    // fp16 K and V tile (2 * P * kBox bytes)
+    const int stage = fp8 ? hg * P * kBox : 2 * hg * P * kBox;
+    const int staging = fp8 ? hg * p.mt * 2 * P * kBox + 1024 : 0;
+    int ns = (200 * 1024 - staging) / stage;
     p.stages = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
     p.threads = (hg * p.mt + 1) * 32;
   }
@@ -559,7 +827,8 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
     if (!f32) {
       const int regs = decode_regs(d);
       const int P = d / 64;
-      const long long smem = 1024 + p.stages * (2LL * p.hg * P * kBox) + 64;
+      const long long smem = 1024 + p.stages * ((fp8 ? 1LL : 2LL) * p.hg * P * kBox) + 64 +
+                             (fp8 ? p.hg * p.mt * 2LL * P * kBox + 1024 : 0);
       long long cps = kSmemPerSm / (smem + 1024);
       const long long cps_regs = 65536 / (static_cast<long long>(p.threads) * regs);
       cps = cps < cps_regs ? cps : cps_regs;
@@ -578,8 +847,9 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
   p.num_splits = (eff + chunk - 1) / chunk;
   if (!f32) {
     const int P = d / 64;
-    const size_t stage = 2ull * p.hg * P * kBox;
+    const size_t stage = (fp8 ? 1ull : 2ull) * p.hg * P * kBox;
     p.smem = 1024 + p.stages * stage + 16ull * p.stages + 4ull * p.stages + 4ull * chunk + 16;
+    if (fp8) p.smem += 1024 + static_cast<size_t>(p.hg) * p.mt * 2 * P * kBox;  // aligned tiles
   }
   if (p.num_splits > 1) {
     const size_t n = static_cast<size_t>(B) * Hq * p.num_splits;
@@ -620,6 +890,27 @@ cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodePlan& p, const C
     ensure_smem_attr<64>(p.smem);
     decode_bf16_kernel<64><<<grid, p.threads, p.smem, s>>>(kmap, vmap, a, p.chunk, p.num_splits,
                                                            p.hg, p.mt, p.stages);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.num_splits <= 1) return e;
+  if (a.d == 128) return launch_merge(decode_merge_kernel<__nv_bfloat16, 128>, a, p, s);
+  return launch_merge(decode_merge_kernel<__nv_bfloat16, 64>, a, p, s);
+}
+
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const DecodePlan& p, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, const float* k_scale,
+                              const float* v_scale, cudaStream_t s) {
+  const dim3 grid(p.num_splits, p.head_chunks, a.B);
+  if (a.d == 128) {
+    ensure_smem_attr_fp8<128>(p.smem);
+    decode_fp8_kernel<128><<<grid, p.threads, p.smem, s>>>(kmap, vmap, a, k_scale, v_scale,
+                                                           p.chunk, p.num_splits, p.hg, p.mt,
+                                                           p.stages);
+  } else {
+    ensure_smem_attr_fp8<64>(p.smem);
+    decode_fp8_kernel<64><<<grid, p.threads, p.smem, s>>>(kmap, vmap, a, k_scale, v_scale,
+                                                          p.chunk, p.num_splits, p.hg, p.mt,
+                                                          p.stages);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.num_splits <= 1) return e;

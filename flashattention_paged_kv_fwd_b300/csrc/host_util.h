@@ -92,6 +92,27 @@ bool encode_pool(CUtensorMap* m, const void* ptr, int d, int heads, int block_si
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// FP8 pool [num_blocks, block_size, heads, d] of 1-byte codes, dimensions in
+// the order (d, token, head, block), boxes of d x block_size x box_heads x 1
+// landing unswizzled as [box_heads][block_size][d] bytes.
+bool encode_pool_u8(CUtensorMap* m, const void* ptr, int d, int heads, int block_size,
+                    int num_blocks, int box_heads) {
+  EncodeFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(block_size),
+                              static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(heads) * d,
+                                 static_cast<cuuint64_t>(d),
+                                 static_cast<cuuint64_t>(block_size) * heads * d};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(d), static_cast<cuuint32_t>(block_size),
+                             static_cast<cuuint32_t>(box_heads), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 double softmax_scale(float scale, int d) {
   return scale > 0.f ? static_cast<double>(scale) : 1.0 / std::sqrt(static_cast<double>(d));
 }

@@ -43,7 +43,7 @@ struct DecodePlan {
 };
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_size, int window,
-                       int num_splits_req, int sm_count, bool f32);
+                       int num_splits_req, int sm_count, bool f32, bool fp8 = false);
 
 struct DecodeArgs {
   const void* q;
@@ -64,6 +64,17 @@ struct DecodeArgs {
 cudaError_t launch_decode_bf16(const DecodeArgs& a, const DecodePlan& p, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s);
+// FP8 (E4M3) pools [num_blocks, 16, Hkv, d] of codes; kmap / vmap are uint8
+// maps ordered (d, token, head, block) with d x 16 x hg x 1 boxes.
+cudaError_t launch_decode_fp8(const DecodeArgs& a, const DecodePlan& p, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, const float* k_scale,
+                              const float* v_scale, cudaStream_t s);
+// Quantise new bf16 rows with their heads' scales into FP8 pools.
+cudaError_t launch_kv_append_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                 void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* table, int max_blocks, const int32_t* seq_lens,
+                                 const int32_t* cu_new, int n_tok, int n_seq, int Hkv, int d,
+                                 int block_size, int num_blocks, int32_t* err, cudaStream_t s);
 
 // ----------------------------------------------------------------- prefill
 struct PrefillArgs {

@@ -26,6 +26,9 @@ Named workloads (sizes as in the model shapes they imitate):
                           U[512, 4096] (packed, causal) plus 240 decode
                           requests with cached lengths U[1, 16384]; all new
                           tokens are appended to one shared pool.
+* ``gqa_decode_llama3_70b_fp8`` the Llama-3-70B-shaped decode over an FP8
+                          cache: the same lengths and table, E4M3 codes drawn
+                          directly (below) and per-head scales U[0.5, 1].
 * ``mla_decode_deepseek_v2`` MLA decode with DeepSeek-V2's latent sizes
                           (d_c = 512, d_R = 64, head_dim 128) and its 128
                           heads split 8 ways (16 heads per GPU): B=64, cached
@@ -50,6 +53,9 @@ __all__ = [
     "chunked_prefill_llama3_8b",
     "make_mla_cache",
     "mla_decode_deepseek_v2",
+    "make_fp8_codes",
+    "make_paged_cache_fp8",
+    "gqa_decode_llama3_70b_fp8",
     "WORKLOADS",
 ]
 
@@ -65,6 +71,7 @@ WORKLOAD_SEEDS = {
     "chunked_prefill_llama3_8b": 1005,
     "cow_copy_blocks_llama3_8b": 1006,
     "mla_decode_deepseek_v2": 1007,
+    "gqa_decode_llama3_70b_fp8": 1008,
 }
 
 
@@ -321,3 +328,69 @@ WORKLOADS = {
     "chunked_prefill_llama3_8b": chunked_prefill_llama3_8b,
     "mla_decode_deepseek_v2": mla_decode_deepseek_v2,
 }
+
+
+# ------------------------------------------------------------- FP8 caches
+FP8_NAN_CODE = 0x7F  # E4M3 S.1111.111
+
+
+def make_fp8_codes(shape, gen, device="cpu"):
+    """E4M3 codes drawn as integers: a random sign, exponent field U[3, 8]
+    and mantissa U[0, 7], i.e. magnitudes between 2^-4 and 3.75, the range of
+    N(0, 1) draws (a plain integer draw; no quantisation happens here)."""
+    sign = torch.randint(0, 2, shape, generator=gen, device=device, dtype=torch.int32) << 7
+    exp = torch.randint(3, 9, shape, generator=gen, device=device, dtype=torch.int32) << 3
+    man = torch.randint(0, 8, shape, generator=gen, device=device, dtype=torch.int32)
+    return (sign | exp | man).to(torch.uint8)
+
+
+def make_paged_cache_fp8(capacities, filled, hkv, d, seed, device="cpu",
+                         block_size=BLOCK_SIZE, poison=True, spare_blocks=0):
+    """make_paged_cache's table and layout for pools of E4M3 codes (uint8),
+    with per-KV-head scales k_scale, v_scale ~ U[0.5, 1] (float32), so the
+    dequantised values stay within +-3.75. Slots that hold no token carry the
+    NaN code when ``poison``."""
+    gen = make_generator(seed, device)
+    cpu_gen = make_generator(seed + 7919, "cpu")
+    nblk = [math.ceil(c / block_size) for c in capacities]
+    num_blocks = max(sum(nblk) + spare_blocks, 1)
+    width = max(max(nblk, default=1), 1)
+    perm = torch.randperm(num_blocks, generator=cpu_gen)
+    table = torch.full((len(capacities), width), -1, dtype=torch.int32)
+    nxt = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[nxt:nxt + n].to(torch.int32)
+        nxt += n
+    k_cache = make_fp8_codes((num_blocks, block_size, hkv, d), gen, device)
+    v_cache = make_fp8_codes((num_blocks, block_size, hkv, d), gen, device)
+    if poison:
+        valid = torch.zeros((num_blocks, block_size), dtype=torch.bool)
+        for b, f in enumerate(filled):
+            nfull = f // block_size
+            if nfull:
+                valid[table[b, :nfull].long()] = True
+            rem = f % block_size
+            if rem:
+                valid[int(table[b, nfull]), :rem] = True
+        invalid = (~valid).to(device)
+        k_cache[invalid] = FP8_NAN_CODE
+        v_cache[invalid] = FP8_NAN_CODE
+    k_scale = (torch.rand((hkv,), generator=gen, device=device) * 0.5 + 0.5).float()
+    v_scale = (torch.rand((hkv,), generator=gen, device=device) * 0.5 + 0.5).float()
+    return {"k_cache": k_cache, "v_cache": v_cache, "k_scale": k_scale, "v_scale": v_scale,
+            "block_table": table.to(device), "num_blocks": num_blocks}
+
+
+def gqa_decode_llama3_70b_fp8(device="cpu", poison=True, batch=64, lo=1024, hi=32768):
+    """The Llama-3-70B-shaped decode (Hq=64, Hkv=8, d=128, lengths
+    U[1024, 32768] from that workload's seed) over an FP8 cache."""
+    seed = WORKLOAD_SEEDS["gqa_decode_llama3_70b_fp8"]
+    lengths = _uniform_ints(lo, hi, batch, make_generator(WORKLOAD_SEEDS["gqa_decode_llama3_70b"] + 2))
+    gen = make_generator(seed, device)
+    q = randn((batch, 64, 128), torch.bfloat16, gen, device)
+    cache = make_paged_cache_fp8(lengths, lengths, 8, 128, seed + 1, device, poison=poison)
+    out = {"q": q, "seq_lens": torch.tensor(lengths, dtype=torch.int32, device=device),
+           "lengths": lengths, "hq": 64, "hkv": 8, "d": 128, "window": 0,
+           "scale": 1.0 / math.sqrt(128)}
+    out.update(cache)
+    return out

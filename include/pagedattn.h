@@ -341,13 +341,61 @@ PA_API int pa_attn_decode_paged(const void* q, const void* k_cache, const void* 
                          pa_dtype dtype, int32_t* err_flag, void* stream);
 
 /*
- * Workspace bytes attn_decode_paged needs for these arguments (0 when every
- * sequence fits one range). Host-only arithmetic except that num_splits = 0
+ * Workspace bytes attn_decode_paged (or attn_decode_paged_fp8) needs for these
+ * arguments (0 when every sequence fits one range). Host-only arithmetic
+ * except that num_splits = 0
  * reads the current device's SM count and the decode kernel's register count
  * (both cached per device). Returns 0 on invalid arguments too.
  */
 PA_API size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int max_blocks_per_seq,
                                  int block_size, int window, int num_splits);
+
+/*
+ * FP8 key/value cache. "Генерация и KV-кэш", section "Сколько весит KV-кэш"
+ * (one byte per cached number in FP8 instead of two in BF16) and section "Как
+ * уменьшить кэш" (the byte lever); "Cache KV, atención flash ..." (a serving
+ * engine started with an FP8 KV cache). The pages fix neither the format nor
+ * the scaling; this library reads them as:
+ *  - codes: E4M3 (OCP 8-bit floating point: sign, 4 exponent bits with bias 7,
+ *    3 mantissa bits, no infinities, largest finite value 448), one byte per
+ *    element, pools [num_blocks, block_size, Hkv, d] of uint8 like the bf16
+ *    pools;
+ *  - scales: k_scale[Hkv] and v_scale[Hkv], float32 device arrays; a code q of
+ *    KV head h stands for value(q) * scale[h].
+ */
+
+/*
+ * kv_append_paged_fp8 -- kv_append_paged into FP8 pools: each new bf16 row
+ * element x of KV head h is stored as the E4M3 code nearest to
+ * float32(x) / scale[h] (IEEE division; ties to the even mantissa; beyond
+ * +-448 it saturates to +-448; NaN stays NaN). Placement, arguments and
+ * error reporting as kv_append_paged (k_new / v_new bf16 [num_new_tokens,
+ * Hkv, d]; pools uint8). Alignment: k_new, v_new 16 bytes; pools 8 bytes.
+ */
+PA_API int pa_kv_append_paged_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                  void* v_cache, const float* k_scale, const float* v_scale,
+                                  const int32_t* block_table, int max_blocks_per_seq,
+                                  const int32_t* seq_lens, const int32_t* cu_new,
+                                  int num_new_tokens, int B, int Hkv, int d, int block_size,
+                                  int num_blocks, int32_t* err_flag, void* stream);
+
+/*
+ * attn_decode_paged_fp8 -- attn_decode_paged over FP8 pools: the attention of
+ * each query over the dequantised keys and values value(q) * scale[h]. q and o
+ * are bf16; the keys and values are converted exactly to fp16 on chip and the
+ * query is rounded to fp16 (exact for bf16 values of magnitude 2^-14 .. 65504)
+ * for the warp MMAs; the key scale is folded into the head's softmax scale and
+ * the value scale into its output; fp32 accumulation. Arguments, workspace
+ * (size it with pa_decode_workspace_bytes) and errors as attn_decode_paged;
+ * block_size must be 16. Alignment: q, o, pools 16 bytes; workspace 256.
+ */
+PA_API int pa_attn_decode_paged_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                    const float* k_scale, const float* v_scale,
+                                    const int32_t* block_table, int max_blocks_per_seq,
+                                    const int32_t* seq_lens, void* o, float* lse, int B, int Hq,
+                                    int Hkv, int d, int block_size, int num_blocks, int window,
+                                    float scale, int num_splits, void* workspace,
+                                    size_t workspace_bytes, int32_t* err_flag, void* stream);
 
 /* Bytes of the library's built-in decode scratch (see below): 32 MiB. */
 #define PA_NOALLOC_SCRATCH_BYTES (32 * 1024 * 1024)
