@@ -17,7 +17,8 @@ first half of the metric; the prefill phase's TFLOP/s (algorithmic causal
 FLOPs, 4*d per visible query-key pair and query head) is the second half,
 under ``prefill``. Timing: CUDA events on the launching stream around each
 phase of each step, L2 flushed before every step (512 MB written, then 256 MB
-of another buffer read, so that L2 holds neither inputs nor dirty lines).
+of another buffer read, so that L2 holds neither inputs nor dirty lines); a
+phase's time is the median over the timed steps.
 
 ``--impl reference`` times the CPU oracle (fp64, full score rows, naive block
 table walk) on a bounded sample of the same workload instead.
@@ -632,7 +633,7 @@ def time_workloads(names, args, dev, binding, flush, stream, world, peaks, peak_
             time_steps(call, [st.phase], 5, flush, stream)
         t = time_steps(call, [st.phase], args.steps, flush, stream)[st.phase]
         binding.check_err_flag(st.err)
-        ms = sum(t) / len(t)
+        ms = statistics.median(t)
         ms, _ = max_over_ranks({st.phase: ms}, ms, dev)
         ms = ms[st.phase]
         work = phase_work(st, st.phase)
@@ -725,7 +726,9 @@ def run_ours(args):
     clocks = sampler.stop()
     binding.check_err_flag(st.err)
 
-    phase_ms = {ph: sum(v) / len(v) for ph, v in times.items()}
+    # per phase the median over the timed steps (a few slow outliers cannot
+    # move it), the step the sum of the phases
+    phase_ms = {ph: statistics.median(v) for ph, v in times.items()}
     step_ms = sum(phase_ms.values())
     phase_ms, step_ms = max_over_ranks(phase_ms, step_ms, dev)
 
