@@ -32,6 +32,7 @@
 //    their V rows zeroed, so unused slots of a block may hold anything.
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -81,20 +82,13 @@ constexpr int kSmemPerSm = 228 * 1024;  // shared memory per SM (planner input)
 // consumer warp: S = Q K^T on the tensor cores, the mask of tokens outside
 // [first visible, seq_len), the online softmax update (log2 domain) and
 // O += P V. kb / vb: the page's K / V tile of this head in shared memory
-// (64-column panel p at + p * hg * kBox), 128-byte swizzled. F16: the tiles,
-// the query fragments and P are fp16 (the FP8 cache's path), else bf16.
-template <int D, bool F16>
+// (64-column panel p at + p * hg * kBox), 128-byte swizzled.
+template <int D>
 __device__ __forceinline__ void consume_page(const uint32_t (&qa)[D / 16][4], uint32_t kb,
                                              uint32_t vb, int hg, int tok0, const SeqRange& r,
                                              float sl2, int mi, int tq, int ktok, int vtok,
                                              float& m0, float& m1, float& l0, float& l1,
                                              float (&acc)[D / 8][4]) {
-  auto mma = [](float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    if constexpr (F16)
-      mma_f16_16816(c, a, b0, b1);
-    else
-      mma_bf16_16816(c, a, b0, b1);
-  };
   float sc[2][4];
 #pragma unroll
   for (int t = 0; t < 2; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
@@ -104,8 +98,8 @@ __device__ __forceinline__ void consume_page(const uint32_t (&qa)[D / 16][4], ui
     const uint32_t addr = kb + (c >> 3) * hg * kBox + ktok * 128 + (((c & 7) ^ (ktok & 7)) << 4);
     uint32_t b0, b1, b2, b3;
     ldsm_x4(addr, b0, b1, b2, b3);
-    mma(sc[0], qa[kk], b0, b1);
-    mma(sc[1], qa[kk], b2, b3);
+    mma_bf16_16816(sc[0], qa[kk], b0, b1);
+    mma_bf16_16816(sc[1], qa[kk], b2, b3);
   }
 
   const bool edge = (tok0 + kBlk > r.len) || (tok0 < r.t_begin);
@@ -154,22 +148,16 @@ __device__ __forceinline__ void consume_page(const uint32_t (&qa)[D / 16][4], ui
     acc[j][2] *= al1;
     acc[j][3] *= al1;
   }
-  auto pack = [](float lo, float hi) {
-    if constexpr (F16)
-      return pack_f16(lo, hi);
-    else
-      return pack_bf16(lo, hi);
-  };
-  const uint32_t pa[4] = {pack(ps[0][0], ps[0][1]), pack(ps[0][2], ps[0][3]),
-                          pack(ps[1][0], ps[1][1]), pack(ps[1][2], ps[1][3])};
+  const uint32_t pa[4] = {pack_bf16(ps[0][0], ps[0][1]), pack_bf16(ps[0][2], ps[0][3]),
+                          pack_bf16(ps[1][0], ps[1][1]), pack_bf16(ps[1][2], ps[1][3])};
 #pragma unroll
   for (int jj = 0; jj < D / 16; ++jj) {
     const int c = jj * 2 + (mi >> 1);
     const uint32_t addr = vb + (c >> 3) * hg * kBox + vtok * 128 + (((c & 7) ^ (vtok & 7)) << 4);
     uint32_t v0, v1, v2, v3;
     ldsm_x4_t(addr, v0, v1, v2, v3);
-    mma(acc[2 * jj], pa, v0 & mlo, v1 & mhi);
-    mma(acc[2 * jj + 1], pa, v2 & mlo, v3 & mhi);
+    mma_bf16_16816(acc[2 * jj], pa, v0 & mlo, v1 & mhi);
+    mma_bf16_16816(acc[2 * jj + 1], pa, v2 & mlo, v3 & mhi);
   }
 }
 
@@ -312,7 +300,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     const int phys = phys_s[st];
     if (phys >= 0)
-      consume_page<D, false>(qa, base + st * stage_bytes + g * kBox,
+      consume_page<D>(qa, base + st * stage_bytes + g * kBox,
                              base + st * stage_bytes + (P * hg + g) * kBox, hg,
                              (pstart + i) * kBlk, r, sl2, mi, tq, ktok, vtok, m0, m1, l0, l1, acc);
     __syncwarp();
@@ -353,14 +341,168 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
 // ------------------------------------------------------- FP8 (E4M3) cache path
 // The same decode over pools of E4M3 codes with one fp32 scale per KV head for
 // keys and one for values (a code q stands for value(q) * scale). A page's
-// codes arrive by TMA (one box of 16 tokens x hg heads x d bytes for K and one
-// for V: half the bytes of the bf16 path). Each consumer warp converts its own
-// head's K and V tiles to fp16 -- every E4M3 value is an fp16 value, one
-// conversion per pair -- into a private tile in the swizzled layout of the bf16
-// path, releases the stage, and runs the same page update with fp16 warp MMAs
-// (the query is rounded to fp16 once, exactly for bf16 values of magnitude
-// 2^-14 .. 65504). The key scale is folded into the softmax scale of the
-// head and the value scale into its output, so no element is rescaled.
+// codes arrive by TMA: one box of d bytes x 16 tokens x hg heads for K and one
+// for V (half the bytes of the bf16 path), swizzled in 16-byte pieces (the
+// 128-byte pattern for d = 128, the 64-byte one for d = 64). Each consumer warp
+// builds its MMA operands straight from the codes in registers: every E4M3
+// value is an fp16 value, so one conversion per pair of codes gives one fp16
+// pair, and no fp16 copy of a page is ever written to shared memory (that copy
+// cost five bytes of shared-memory traffic per byte of cache).
+//  * K is the B operand of S = Q K^T, contracted over the head dims. A dot
+//    product does not depend on the order of its terms, so lane (n, c) reads
+//    16 whole bytes of its key row with one 128-bit load and feeds 4 of them
+//    to each of four k-steps; the query fragments are loaded in that same dim
+//    order.
+//  * V is the B operand of O += P V, contracted over the keys: an MMA register
+//    pairs two keys of one dim. A lane loads 4 bytes (4 dims) from each of its
+//    4 key rows and interleaves two rows' bytes with byte permutes. Dim tile
+//    4u + t of the output holds dims 32u + 4n + t in its column n, so a lane
+//    ends with 8 consecutive dims of O per row.
+//  * Column n of an 8-key score tile is page row fp8_key_row(n) (+8 for the
+//    second tile). With this order and the swizzle neither load has a bank
+//    conflict (checked for both head dims).
+// The query is rounded to fp16 once (exact for bf16 values of magnitude
+// 2^-14 .. 65504). The key scale is folded into the softmax scale of the head
+// and the value scale into its output, so no element is rescaled.
+
+// Page row of column n of an 8-key score tile: 0, 7, 3, 4, 5, 2, 6, 1. Rows of
+// columns 2m and 2m + 1 differ in bits 0 and 2 (the K loads of a quarter warp
+// cover distinct banks); the rows of even columns, and of odd ones, differ in
+// bits 1-2 and in bits 0 and 2 (the V loads of a warp cover distinct banks).
+__device__ __forceinline__ int fp8_key_row(int n) { return (0x16254370u >> (4 * n)) & 0xFu; }
+
+// XOR pattern of the tensor copy's swizzle for byte offsets in page row `row`
+// of a head tile of 16 rows x D bytes (tile base aligned to the pattern's
+// period): 16-byte piece p of the row sits at piece p ^ pattern.
+template <int D>
+__device__ __forceinline__ uint32_t fp8_row_swz(int row) {
+  if constexpr (D == 128)
+    return static_cast<uint32_t>(row & 7) << 4;
+  else
+    return static_cast<uint32_t>((row >> 1) & 3) << 4;
+}
+
+// One page (16 tokens) of one KV head for the 16 query-head rows of a
+// consumer warp, over the page's code tiles kt / vt (shared addresses).
+template <int D>
+__device__ __forceinline__ void consume_page_fp8(const uint32_t (&qa)[D / 16][4], uint32_t kt,
+                                                 uint32_t vt, int tok0, const SeqRange& r,
+                                                 float sl2, int gr, int tq, float& m0, float& m1,
+                                                 float& l0, float& l1, float (&acc)[D / 8][4]) {
+  float sc[2][4];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+  {
+    // this lane's key rows in the two score tiles, and its 16-byte piece
+    const int k0 = fp8_key_row(gr), k1 = 8 + k0;
+    const uint32_t a0 = kt + k0 * D + ((16u * tq) ^ fp8_row_swz<D>(k0));
+    const uint32_t a1 = kt + k1 * D + ((16u * tq) ^ fp8_row_swz<D>(k1));
+#pragma unroll
+    for (int qc = 0; qc < D / 64; ++qc) {
+      // qc > 0 only for D = 128, whose rows are 128-byte aligned: bit 6 of the
+      // address is bit 6 of the in-row offset, and XOR commutes with the swizzle
+      uint32_t w0[4], w1[4];
+      lds_v4(a0 ^ (64u * qc), w0);
+      lds_v4(a1 ^ (64u * qc), w1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        mma_f16_16816(sc[0], qa[4 * qc + j], e4m3x2_to_f16x2(static_cast<uint16_t>(w0[j])),
+                      e4m3x2_to_f16x2(static_cast<uint16_t>(w0[j] >> 16)));
+        mma_f16_16816(sc[1], qa[4 * qc + j], e4m3x2_to_f16x2(static_cast<uint16_t>(w1[j])),
+                      e4m3x2_to_f16x2(static_cast<uint16_t>(w1[j] >> 16)));
+      }
+    }
+  }
+
+  // rows of this lane's score columns 2 tq and 2 tq + 1 (and +8 in tile 1)
+  const int ra = fp8_key_row(2 * tq), rb = fp8_key_row(2 * tq + 1);
+  const bool edge = (tok0 + kBlk > r.len) || (tok0 < r.t_begin);
+  uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
+  if (edge) {
+    auto ok = [&](int tok) { return tok < r.len && tok >= r.t_begin; };
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (!ok(tok0 + 8 * t + ((e & 1) ? rb : ra))) sc[t][e] = kNegInf;
+    mlo = (ok(tok0 + ra) ? 0x0000FFFFu : 0u) | (ok(tok0 + rb) ? 0xFFFF0000u : 0u);
+    mhi = (ok(tok0 + 8 + ra) ? 0x0000FFFFu : 0u) | (ok(tok0 + 8 + rb) ? 0xFFFF0000u : 0u);
+  }
+
+  // online softmax (log2 domain), rows gr (e = 0,1) and gr + 8 (e = 2,3)
+  float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) * sl2;
+  float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])) * sl2;
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+  const float mu0 = mn0 == kNegInf ? 0.f : mn0;
+  const float mu1 = mn1 == kNegInf ? 0.f : mn1;
+  const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
+  m0 = mn0;
+  m1 = mn1;
+  float ps[2][4];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    ps[t][0] = ex2(fmaf(sc[t][0], sl2, -mu0));
+    ps[t][1] = ex2(fmaf(sc[t][1], sl2, -mu0));
+    ps[t][2] = ex2(fmaf(sc[t][2], sl2, -mu1));
+    ps[t][3] = ex2(fmaf(sc[t][3], sl2, -mu1));
+  }
+  l0 = l0 * al0 + (ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1]);
+  l1 = l1 * al1 + (ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3]);
+  // the factors are exactly 1 unless a row's max moved, which gets rare as
+  // keys accumulate: skip the multiplies when no row of the warp needs them
+  if (__any_sync(0xFFFFFFFFu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      acc[j][0] *= al0;
+      acc[j][1] *= al0;
+      acc[j][2] *= al1;
+      acc[j][3] *= al1;
+    }
+  }
+  const uint32_t pa[4] = {pack_f16(ps[0][0], ps[0][1]), pack_f16(ps[0][2], ps[0][3]),
+                          pack_f16(ps[1][0], ps[1][1]), pack_f16(ps[1][2], ps[1][3])};
+
+  // V rows ra, rb (low / high half of b0) and 8 + ra, 8 + rb (of b1); this
+  // lane's 4 bytes of dim group u are dims 32u + 4 gr .. + 3
+  const uint32_t va = vt + ra * D + ((4u * gr) ^ fp8_row_swz<D>(ra));
+  const uint32_t vb = vt + rb * D + ((4u * gr) ^ fp8_row_swz<D>(rb));
+  const uint32_t vc = vt + (8 + ra) * D + ((4u * gr) ^ fp8_row_swz<D>(8 + ra));
+  const uint32_t vd = vt + (8 + rb) * D + ((4u * gr) ^ fp8_row_swz<D>(8 + rb));
+  // edge pages zero the V rows of masked keys (P = 0 times a NaN code is NaN);
+  // the others skip the masking
+  auto pv = [&](auto masked) {
+#pragma unroll
+    for (int u = 0; u < D / 32; ++u) {
+      // 32u sets bits 5-6 of the in-row offset, which the swizzle XORs: apply
+      // the group's offset with XOR as well (4 gr only occupies bits 2-4)
+      const uint32_t wa = lds_u32(va ^ (32u * u)), wb = lds_u32(vb ^ (32u * u));
+      const uint32_t wc = lds_u32(vc ^ (32u * u)), wd = lds_u32(vd ^ (32u * u));
+      const uint32_t p01 = __byte_perm(wa, wb, 0x5140), p23 = __byte_perm(wa, wb, 0x7362);
+      const uint32_t q01 = __byte_perm(wc, wd, 0x5140), q23 = __byte_perm(wc, wd, 0x7362);
+      auto lo = [&](uint32_t w, uint32_t m) {
+        const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(w));
+        return decltype(masked)::value ? h & m : h;
+      };
+      auto hi = [&](uint32_t w, uint32_t m) {
+        const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+        return decltype(masked)::value ? h & m : h;
+      };
+      mma_f16_16816(acc[4 * u + 0], pa, lo(p01, mlo), lo(q01, mhi));
+      mma_f16_16816(acc[4 * u + 1], pa, hi(p01, mlo), hi(q01, mhi));
+      mma_f16_16816(acc[4 * u + 2], pa, lo(p23, mlo), lo(q23, mhi));
+      mma_f16_16816(acc[4 * u + 3], pa, hi(p23, mlo), hi(q23, mhi));
+    }
+  };
+  if (edge)
+    pv(std::true_type{});
+  else
+    pv(std::false_type{});
+}
+
 template <int D>
 __global__ void __launch_bounds__((kMaxConsumerWarps<D> + 1) * 32, 1)
 decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -368,7 +510,6 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
                   const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                   const int chunk, const int num_splits, const int hg, const int mt,
                   const int ns) {
-  constexpr int P = D / 64;
   const int G = a.Hq / a.Hkv;
   const int b = blockIdx.z, hc = blockIdx.y, s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -395,14 +536,13 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t stage_bytes = 2u * hg * kBlk * D;  // K codes [hg][16][D], then V codes
+  // K codes [hg][16][D], then V codes: head tiles of 1 or 2 KB on 1024-byte
+  // boundaries, as the swizzle pattern needs
+  const uint32_t stage_bytes = 2u * hg * kBlk * D;
   const uint32_t bars = base + ns * stage_bytes;  // full[ns], empty[ns]
   int32_t* phys_s = reinterpret_cast<int32_t*>(gbase + ns * stage_bytes + 16 * ns);
   int32_t* tab_s = phys_s + ns;
   volatile int32_t* abort_s = tab_s + chunk;
-  // per-warp fp16 tiles: K panels then V panels, 16 tokens x 128 bytes each
-  const uint32_t stg0 =
-      (smem_u32(const_cast<const int32_t*>(abort_s) + 1) + 1023u) & ~1023u;
   auto full = [&](int i) { return bars + 8u * i; };
   auto empty = [&](int i) { return bars + 8u * (ns + i); };
 
@@ -465,10 +605,10 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
   const int gr = lane >> 2, tq = lane & 3;
   const float sl2 = a.scale_log2 * k_scale[kvh];
   const float vsc = v_scale[kvh];
-  const uint32_t stg_k = stg0 + static_cast<uint32_t>(warp * 2 * P * kBox);
-  const uint32_t stg_v = stg_k + P * kBox;
 
-  // query fragments, rounded to fp16
+  // query fragments, rounded to fp16, in the dim order of the K reads: k-step
+  // 4 qc + j takes dims 64 qc + 16 tq + 4 j + {0, 1} (k = 2 tq, 2 tq + 1) and
+  // + {2, 3} (k = 2 tq + 8, 2 tq + 9)
   uint32_t qa[D / 16][4];
   {
     const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
@@ -478,12 +618,15 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
       return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
     };
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      qa[kk][0] = gr < nrows ? h2(q32[ra + kk * 8 + tq]) : 0u;
-      qa[kk][1] = gr + 8 < nrows ? h2(q32[rb + kk * 8 + tq]) : 0u;
-      qa[kk][2] = gr < nrows ? h2(q32[ra + kk * 8 + 4 + tq]) : 0u;
-      qa[kk][3] = gr + 8 < nrows ? h2(q32[rb + kk * 8 + 4 + tq]) : 0u;
-    }
+    for (int qc = 0; qc < D / 64; ++qc)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int w = 32 * qc + 8 * tq + 2 * j;  // word w holds dims 2w, 2w + 1
+        qa[4 * qc + j][0] = gr < nrows ? h2(q32[ra + w]) : 0u;
+        qa[4 * qc + j][1] = gr + 8 < nrows ? h2(q32[rb + w]) : 0u;
+        qa[4 * qc + j][2] = gr < nrows ? h2(q32[ra + w + 1]) : 0u;
+        qa[4 * qc + j][3] = gr + 8 < nrows ? h2(q32[rb + w + 1]) : 0u;
+      }
   }
 
   float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
@@ -491,12 +634,9 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  const int mi = lane >> 3, rr = lane & 7;
-  const int ktok = ((mi >> 1) << 3) + rr;
-  const int vtok = ((mi & 1) << 3) + rr;
-
   for (int i = 0; i < npg; ++i) {
     const int st = i % ns;
+    // warp-uniform outcome: the mma.sync below need all 32 lanes
     if (!__all_sync(0xFFFFFFFFu, mbar_wait(full(st), (i / ns) & 1, a.wait_ns))) {
       if (lane == 0) raise_err(a.err, kDevErrTimeout);
       *abort_s = 1;
@@ -504,49 +644,17 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     const int phys = phys_s[st];
     if (phys >= 0) {
-      // lane i takes bytes [512 j + 16 i, +16) of the head's 16 x D tile of
-      // codes: consecutive lanes read consecutive 16-byte pieces (no bank
-      // conflicts), each covering 16 elements of one token row
-      const uint8_t* tile = gbase + st * stage_bytes + static_cast<uint32_t>(g * kBlk * D);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const uint8_t* src = tile + t * (stage_bytes / 2);
-        const uint32_t dst = t ? stg_v : stg_k;
-#pragma unroll
-        for (int j = 0; j < kBlk * D / 512; ++j) {
-          const int off = 512 * j + 16 * lane;
-          const int row = off / D, e0 = off % D;
-          const uint4 w = *reinterpret_cast<const uint4*>(src + off);
-          const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
-          uint32_t h[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            h[2 * e] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws4[e] & 0xFFFFu));
-            h[2 * e + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws4[e] >> 16));
-          }
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int el = e0 + 8 * half;
-            const int p = el >> 6, c = (el & 63) >> 3;
-            const uint32_t addr =
-                dst + p * kBox + row * 128 + ((static_cast<uint32_t>(c) ^ (row & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                         "r"(h[4 * half]), "r"(h[4 * half + 1]), "r"(h[4 * half + 2]),
-                         "r"(h[4 * half + 3])
-                         : "memory");
-          }
-        }
-      }
+      const uint32_t kt = base + st * stage_bytes + static_cast<uint32_t>(g * kBlk * D);
+      consume_page_fp8<D>(qa, kt, kt + stage_bytes / 2, (pstart + i) * kBlk, r, sl2, gr, tq, m0,
+                          m1, l0, l1, acc);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty(st));  // the codes are converted: the stage is free
-    if (phys >= 0)
-      consume_page<D, true>(qa, stg_k, stg_v, 1, (pstart + i) * kBlk, r, sl2, mi, tq, ktok, vtok,
-                            m0, m1, l0, l1, acc);
-    __syncwarp();  // every lane is done with the private tiles before the next page
+    if (lane == 0) mbar_arrive(empty(st));
   }
 
   // ------------------------------------------------------------- epilogue
+  // dim 32u + 8 tq + t of a row is acc[4u + t][2 half], dim 32u + 8 tq + 4 + t
+  // is acc[4u + t][2 half + 1]: 8 consecutive dims per lane and group
   l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
   l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
   l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
@@ -561,17 +669,25 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
     const float inv = l > 0.f ? vsc / l : 0.f;
     const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
     const int64_t bh = static_cast<int64_t>(b) * a.Hq + h;
+    const int e0 = 2 * half, e1 = 2 * half + 1;
     if (single) {
-      uint32_t* o32 = static_cast<uint32_t*>(a.o) + bh * (D / 2);
+      uint4* o4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + bh * D);
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j)
-        o32[j * 4 + tq] = pack_bf16(acc[j][2 * half] * inv, acc[j][2 * half + 1] * inv);
+      for (int u = 0; u < D / 32; ++u)
+        o4[4 * u + tq] = make_uint4(pack_bf16(acc[4 * u][e0] * inv, acc[4 * u + 1][e0] * inv),
+                                    pack_bf16(acc[4 * u + 2][e0] * inv, acc[4 * u + 3][e0] * inv),
+                                    pack_bf16(acc[4 * u][e1] * inv, acc[4 * u + 1][e1] * inv),
+                                    pack_bf16(acc[4 * u + 2][e1] * inv, acc[4 * u + 3][e1] * inv));
       if (tq == 0 && a.lse) a.lse[h * a.B + b] = lse_v;
     } else {
-      float2* w = reinterpret_cast<float2*>(a.ws_o + (bh * num_splits + s) * D);
+      float4* w = reinterpret_cast<float4*>(a.ws_o + (bh * num_splits + s) * D);
 #pragma unroll
-      for (int j = 0; j < D / 8; ++j)
-        w[j * 4 + tq] = make_float2(acc[j][2 * half] * inv, acc[j][2 * half + 1] * inv);
+      for (int u = 0; u < D / 32; ++u) {
+        w[8 * u + 2 * tq] = make_float4(acc[4 * u][e0] * inv, acc[4 * u + 1][e0] * inv,
+                                        acc[4 * u + 2][e0] * inv, acc[4 * u + 3][e0] * inv);
+        w[8 * u + 2 * tq + 1] = make_float4(acc[4 * u][e1] * inv, acc[4 * u + 1][e1] * inv,
+                                            acc[4 * u + 2][e1] * inv, acc[4 * u + 3][e1] * inv);
+      }
       if (tq == 0) a.ws_lse[bh * num_splits + s] = lse_v;
     }
   }
@@ -739,18 +855,24 @@ void ensure_smem_attr(size_t bytes) {
   }
 }
 
-// Registers per thread of the bf16 decode kernel as compiled (read once per
-// device), rounded up to the allocation step of 8: the planner's count of
-// CTAs that fit on an SM follows the build instead of a number written down.
-int decode_regs(int d) {
-  static int cached[2][64] = {};
+// Registers per thread of the bf16 (or FP8) decode kernel as compiled (read
+// once per device), rounded up to the allocation step of 8: the planner's
+// count of CTAs that fit on an SM follows the build instead of a number
+// written down.
+int decode_regs(int d, bool fp8) {
+  static int cached[2][2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  int& c = cached[d == 128][dev];
+  int& c = cached[fp8][d == 128][dev];
   if (!c) {
     cudaFuncAttributes fa{};
-    const cudaError_t e = d == 128 ? cudaFuncGetAttributes(&fa, decode_bf16_kernel<128>)
-                                   : cudaFuncGetAttributes(&fa, decode_bf16_kernel<64>);
+    cudaError_t e;
+    if (fp8)
+      e = d == 128 ? cudaFuncGetAttributes(&fa, decode_fp8_kernel<128>)
+                   : cudaFuncGetAttributes(&fa, decode_fp8_kernel<64>);
+    else
+      e = d == 128 ? cudaFuncGetAttributes(&fa, decode_bf16_kernel<128>)
+                   : cudaFuncGetAttributes(&fa, decode_bf16_kernel<64>);
     if (e != cudaSuccess || fa.numRegs <= 0) {
       cudaGetLastError();
       return 255;  // unknown: plan as if one CTA per SM
@@ -802,11 +924,9 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
       if (Hkv % c == 0 && c * p.mt <= max_warps && 2 * c * P * kBox <= 64 * 1024) hg = c;
     p.hg = hg;
     p.head_chunks = Hkv / hg;
-    // FP8 pages are half the bytes; each consumer warp also keeps a private
-    // fp16 K and V tile (2 * P * kBox bytes)
+    // FP8 pages are half the bytes
     const int stage = fp8 ? hg * P * kBox : 2 * hg * P * kBox;
-    const int staging = fp8 ? hg * p.mt * 2 * P * kBox + 1024 : 0;
-    int ns = (200 * 1024 - staging) / stage;
+    int ns = 200 * 1024 / stage;
     p.stages = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
     p.threads = (hg * p.mt + 1) * 32;
   }
@@ -825,10 +945,9 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
     // holds most of an SM's shared memory and registers) runs in one wave
     // instead: the largest range count per sequence that still fits.
     if (!f32) {
-      const int regs = decode_regs(d);
+      const int regs = decode_regs(d, fp8);
       const int P = d / 64;
-      const long long smem = 1024 + p.stages * ((fp8 ? 1LL : 2LL) * p.hg * P * kBox) + 64 +
-                             (fp8 ? p.hg * p.mt * 2LL * P * kBox + 1024 : 0);
+      const long long smem = 1024 + p.stages * ((fp8 ? 1LL : 2LL) * p.hg * P * kBox) + 64;
       long long cps = kSmemPerSm / (smem + 1024);
       const long long cps_regs = 65536 / (static_cast<long long>(p.threads) * regs);
       cps = cps < cps_regs ? cps : cps_regs;
@@ -849,7 +968,6 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
     const int P = d / 64;
     const size_t stage = (fp8 ? 1ull : 2ull) * p.hg * P * kBox;
     p.smem = 1024 + p.stages * stage + 16ull * p.stages + 4ull * p.stages + 4ull * chunk + 16;
-    if (fp8) p.smem += 1024 + static_cast<size_t>(p.hg) * p.mt * 2 * P * kBox;  // aligned tiles
   }
   if (p.num_splits > 1) {
     const size_t n = static_cast<size_t>(B) * Hq * p.num_splits;

@@ -94,7 +94,9 @@ bool encode_pool(CUtensorMap* m, const void* ptr, int d, int heads, int block_si
 
 // FP8 pool [num_blocks, block_size, heads, d] of 1-byte codes, dimensions in
 // the order (d, token, head, block), boxes of d x block_size x box_heads x 1
-// landing unswizzled as [box_heads][block_size][d] bytes.
+// landing as [box_heads][block_size][d] bytes with the 16-byte pieces of each
+// row swizzled: the 128-byte pattern for d = 128 (piece p of row r at p ^ (r % 8)),
+// the 64-byte one for d = 64 (at p ^ ((r / 2) % 4)).
 bool encode_pool_u8(CUtensorMap* m, const void* ptr, int d, int heads, int block_size,
                     int num_blocks, int box_heads) {
   EncodeFn fn = encode_fn();
@@ -109,7 +111,8 @@ bool encode_pool_u8(CUtensorMap* m, const void* ptr, int d, int heads, int block
                              static_cast<cuuint32_t>(box_heads), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

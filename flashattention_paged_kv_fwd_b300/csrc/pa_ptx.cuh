@@ -347,6 +347,18 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Shared-memory loads at a 32-bit shared address (volatile: they stay after
+// the mbarrier wait that made the bytes visible).
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(addr));
+  return r;
+}
+__device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
 
 // ------------------------------------------- packed fp32 pairs (sm_100 family)
 // Two fp32 lanes in one 64-bit register; one instruction operates on both.
