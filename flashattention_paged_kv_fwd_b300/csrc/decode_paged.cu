@@ -343,32 +343,42 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap kmap,
 // keys and one for values (a code q stands for value(q) * scale). A page's
 // codes arrive by TMA: one box of d bytes x 16 tokens x hg heads for K and one
 // for V (half the bytes of the bf16 path), swizzled in 16-byte pieces (the
-// 128-byte pattern for d = 128, the 64-byte one for d = 64). Each consumer warp
-// builds its MMA operands straight from the codes in registers: every E4M3
-// value is an fp16 value, so one conversion per pair of codes gives one fp16
-// pair, and no fp16 copy of a page is ever written to shared memory (that copy
-// cost five bytes of shared-memory traffic per byte of cache).
-//  * K is the B operand of S = Q K^T, contracted over the head dims. A dot
-//    product does not depend on the order of its terms, so lane (n, c) reads
-//    16 whole bytes of its key row with one 128-bit load and feeds 4 of them
-//    to each of four k-steps; the query fragments are loaded in that same dim
-//    order.
-//  * V is the B operand of O += P V, contracted over the keys: an MMA register
-//    pairs two keys of one dim. A lane loads 4 bytes (4 dims) from each of its
-//    4 key rows and interleaves two rows' bytes with byte permutes. Dim tile
-//    4u + t of the output holds dims 32u + 4n + t in its column n, so a lane
-//    ends with 8 consecutive dims of O per row.
-//  * Column n of an 8-key score tile is page row fp8_key_row(n) (+8 for the
-//    second tile). With this order and the swizzle neither load has a bank
-//    conflict (checked for both head dims).
+// 128-byte pattern for d = 128, the 64-byte one for d = 64). A consumer warp
+// serves up to 8 query heads of one KV head and builds its MMA operands
+// straight from the codes in registers: every E4M3 value is an fp16 value, so
+// one conversion per pair of codes gives one fp16 pair, and no fp16 copy of a
+// page is written to shared memory (that copy cost five bytes of shared-memory
+// traffic per byte of cache). The products are transposed so that the page's
+// 16 keys, not the query heads, are the 16 rows of an m16n8k16 MMA and the
+// heads its 8 columns: no padding rows for Hq / Hkv <= 8, half the MMAs and
+// half the accumulator registers of a heads-as-rows layout.
+//  * S^T = K Q^T. A = the K codes (rows = keys), contracted over the head
+//    dims. A dot product does not depend on the order of its terms, so a lane
+//    reads 16 whole bytes of each of its two key rows with one 128-bit load
+//    and feeds 4 of them to each of four k-steps; the query (the B operand) is
+//    loaded once in that same dim order.
+//  * P^T (keys x heads, fp16) is the S^T accumulator tile as it stands, moved
+//    into B-operand layout by two 8x8 register transposes.
+//  * O^T += V^T P^T. A = V^T (rows = head dims, k = keys): an MMA register
+//    pairs two keys of one dim, so a lane loads 8 bytes (8 dims) of each of its
+//    4 key rows and interleaves two rows' bytes with byte permutes. Row r of
+//    output tile 4u + t is dim 64u + 8 (r % 8) + 4 (r / 8) + t, so a lane ends
+//    with 8 consecutive dims of each of its two heads.
+//  * Row r < 8 of the score tile is page row fp8_key_row(r), row 8 + r is
+//    page row 8 + fp8_key_row(r): with this order and the swizzle neither
+//    load has a bank conflict (checked for both head dims).
 // The query is rounded to fp16 once (exact for bf16 values of magnitude
 // 2^-14 .. 65504). The key scale is folded into the softmax scale of the head
 // and the value scale into its output, so no element is rescaled.
 
-// Page row of column n of an 8-key score tile: 0, 7, 3, 4, 5, 2, 6, 1. Rows of
-// columns 2m and 2m + 1 differ in bits 0 and 2 (the K loads of a quarter warp
-// cover distinct banks); the rows of even columns, and of odd ones, differ in
-// bits 1-2 and in bits 0 and 2 (the V loads of a warp cover distinct banks).
+constexpr int kFp8ConsumerWarps = 8;  // per CTA at most; two CTAs fit on an SM
+
+// Page row of score-tile row n < 8: 0, 7, 3, 4, 5, 2, 6, 1. The K loads of a
+// quarter warp read rows fp8_key_row(2m), fp8_key_row(2m + 1), which differ in
+// bits 0 and 2; the V loads read the rows of even n, or of odd n, across a
+// warp, which differ in bits 1-2 and in bits 0 and 2: with the swizzle below
+// every 16-byte piece a quarter (K) or half (V) warp reads lies in distinct
+// banks.
 __device__ __forceinline__ int fp8_key_row(int n) { return (0x16254370u >> (4 * n)) & 0xFu; }
 
 // XOR pattern of the tensor copy's swizzle for byte offsets in page row `row`
@@ -382,19 +392,46 @@ __device__ __forceinline__ uint32_t fp8_row_swz(int row) {
     return static_cast<uint32_t>((row >> 1) & 3) << 4;
 }
 
-// One page (16 tokens) of one KV head for the 16 query-head rows of a
-// consumer warp, over the page's code tiles kt / vt (shared addresses).
+__device__ __forceinline__ uint32_t e4m3_lo(uint32_t w) {
+  return e4m3x2_to_f16x2(static_cast<uint16_t>(w));
+}
+__device__ __forceinline__ uint32_t e4m3_hi(uint32_t w) {
+  return e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+}
+
+// One page (16 tokens) of one KV head for the up to 8 query heads of a
+// consumer warp, over the page's code tiles kt / vt (shared addresses). Lane
+// (gr, tq) holds the scores of page rows fp8_key_row(gr) and 8 +
+// fp8_key_row(gr) for the warp's heads 2 tq and 2 tq + 1; m[i] and l[i] are
+// the running max (log2 domain) and sum of head 2 tq + i, l over this lane's
+// keys only (summed across the lanes of a head at the end).
 template <int D>
-__device__ __forceinline__ void consume_page_fp8(const uint32_t (&qa)[D / 16][4], uint32_t kt,
+__device__ __forceinline__ void consume_page_fp8(const uint32_t (&qb)[D / 16][2], uint32_t kt,
                                                  uint32_t vt, int tok0, const SeqRange& r,
-                                                 float sl2, int gr, int tq, float& m0, float& m1,
-                                                 float& l0, float& l1, float (&acc)[D / 8][4]) {
-  float sc[2][4];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) sc[t][0] = sc[t][1] = sc[t][2] = sc[t][3] = 0.f;
+                                                 float sl2, int gr, int tq, float (&m)[2],
+                                                 float (&l)[2], float (&acc)[D / 16][4]) {
+  const int k0 = fp8_key_row(gr), k1 = 8 + k0;  // this lane's score rows
+  const int ra = fp8_key_row(2 * tq), rb = fp8_key_row(2 * tq + 1);  // its V rows (and + 8)
+
+  // V first: the loads do not depend on the scores, so their latency hides
+  // behind S. vw[u][i]: 8 bytes (dims 64u + 8 gr .. + 7) of row ra, rb,
+  // 8 + ra, 8 + rb. 64u sets bit 6 of the in-row offset, 8 gr bits 3-5: the
+  // swizzle XORs bits 4-6 and the row bases keep bit 6 clear, so the group
+  // offset is applied with XOR too.
+  uint32_t vw[D / 64][4][2];
   {
-    // this lane's key rows in the two score tiles, and its 16-byte piece
-    const int k0 = fp8_key_row(gr), k1 = 8 + k0;
+    const int rows[4] = {ra, rb, 8 + ra, 8 + rb};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a = vt + rows[i] * D + ((8u * gr) ^ fp8_row_swz<D>(rows[i]));
+#pragma unroll
+      for (int u = 0; u < D / 64; ++u) lds_v2(a ^ (64u * u), vw[u][i][0], vw[u][i][1]);
+    }
+  }
+
+  // S^T, even and odd k-steps in two accumulators (two MMA chains)
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  {
     const uint32_t a0 = kt + k0 * D + ((16u * tq) ^ fp8_row_swz<D>(k0));
     const uint32_t a1 = kt + k1 * D + ((16u * tq) ^ fp8_row_swz<D>(k1));
 #pragma unroll
@@ -406,95 +443,91 @@ __device__ __forceinline__ void consume_page_fp8(const uint32_t (&qa)[D / 16][4]
       lds_v4(a1 ^ (64u * qc), w1);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        mma_f16_16816(sc[0], qa[4 * qc + j], e4m3x2_to_f16x2(static_cast<uint16_t>(w0[j])),
-                      e4m3x2_to_f16x2(static_cast<uint16_t>(w0[j] >> 16)));
-        mma_f16_16816(sc[1], qa[4 * qc + j], e4m3x2_to_f16x2(static_cast<uint16_t>(w1[j])),
-                      e4m3x2_to_f16x2(static_cast<uint16_t>(w1[j] >> 16)));
+        const uint32_t a[4] = {e4m3_lo(w0[j]), e4m3_lo(w1[j]), e4m3_hi(w0[j]), e4m3_hi(w1[j])};
+        if (j & 1)
+          mma_f16_16816(s1, a, qb[4 * qc + j][0], qb[4 * qc + j][1]);
+        else
+          mma_f16_16816(s0, a, qb[4 * qc + j][0], qb[4 * qc + j][1]);
       }
     }
   }
+  // sc[0] / sc[1]: row k0, heads 2 tq / 2 tq + 1; sc[2] / sc[3]: row k1
+  float sc[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sc[e] = s0[e] + s1[e];
 
-  // rows of this lane's score columns 2 tq and 2 tq + 1 (and +8 in tile 1)
-  const int ra = fp8_key_row(2 * tq), rb = fp8_key_row(2 * tq + 1);
   const bool edge = (tok0 + kBlk > r.len) || (tok0 < r.t_begin);
   uint32_t mlo = 0xFFFFFFFFu, mhi = 0xFFFFFFFFu;
   if (edge) {
     auto ok = [&](int tok) { return tok < r.len && tok >= r.t_begin; };
-#pragma unroll
-    for (int t = 0; t < 2; ++t)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (!ok(tok0 + 8 * t + ((e & 1) ? rb : ra))) sc[t][e] = kNegInf;
+    if (!ok(tok0 + k0)) sc[0] = sc[1] = kNegInf;
+    if (!ok(tok0 + k1)) sc[2] = sc[3] = kNegInf;
     mlo = (ok(tok0 + ra) ? 0x0000FFFFu : 0u) | (ok(tok0 + rb) ? 0xFFFF0000u : 0u);
     mhi = (ok(tok0 + 8 + ra) ? 0x0000FFFFu : 0u) | (ok(tok0 + 8 + rb) ? 0xFFFF0000u : 0u);
   }
 
-  // online softmax (log2 domain), rows gr (e = 0,1) and gr + 8 (e = 2,3)
-  float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) * sl2;
-  float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])) * sl2;
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, 2));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 1));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, 2));
-  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+  // online softmax per head (log2 domain): max over the page's 16 keys, i.e.
+  // this lane's two rows and the lanes of other gr
+  float mx0 = fmaxf(sc[0], sc[2]) * sl2, mx1 = fmaxf(sc[1], sc[3]) * sl2;
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+  }
+  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
   const float mu0 = mn0 == kNegInf ? 0.f : mn0;
   const float mu1 = mn1 == kNegInf ? 0.f : mn1;
-  const float al0 = ex2(m0 - mu0), al1 = ex2(m1 - mu1);
-  m0 = mn0;
-  m1 = mn1;
-  float ps[2][4];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    ps[t][0] = ex2(fmaf(sc[t][0], sl2, -mu0));
-    ps[t][1] = ex2(fmaf(sc[t][1], sl2, -mu0));
-    ps[t][2] = ex2(fmaf(sc[t][2], sl2, -mu1));
-    ps[t][3] = ex2(fmaf(sc[t][3], sl2, -mu1));
-  }
-  l0 = l0 * al0 + (ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1]);
-  l1 = l1 * al1 + (ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3]);
-  // the factors are exactly 1 unless a row's max moved, which gets rare as
-  // keys accumulate: skip the multiplies when no row of the warp needs them
+  const float al0 = ex2(m[0] - mu0), al1 = ex2(m[1] - mu1);
+  m[0] = mn0;
+  m[1] = mn1;
+  const float p0 = ex2(fmaf(sc[0], sl2, -mu0)), p1 = ex2(fmaf(sc[1], sl2, -mu1));
+  const float p2 = ex2(fmaf(sc[2], sl2, -mu0)), p3 = ex2(fmaf(sc[3], sl2, -mu1));
+  l[0] = l[0] * al0 + (p0 + p2);
+  l[1] = l[1] * al1 + (p1 + p3);
+  // the factors are exactly 1 unless a head's max moved, which gets rare as
+  // keys accumulate: skip the multiplies when no head of the warp needs them
   if (__any_sync(0xFFFFFFFFu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      acc[j][0] *= al0;
-      acc[j][1] *= al0;
-      acc[j][2] *= al1;
-      acc[j][3] *= al1;
+    for (int t = 0; t < D / 16; ++t) {
+      acc[t][0] *= al0;
+      acc[t][1] *= al1;
+      acc[t][2] *= al0;
+      acc[t][3] *= al1;
     }
   }
-  const uint32_t pa[4] = {pack_f16(ps[0][0], ps[0][1]), pack_f16(ps[0][2], ps[0][3]),
-                          pack_f16(ps[1][0], ps[1][1]), pack_f16(ps[1][2], ps[1][3])};
+  // P^T as the B operand: head gr, score rows 2 tq, 2 tq + 1 (pb0) and
+  // 8 + 2 tq, 8 + 2 tq + 1 (pb1)
+  const uint32_t pb0 = movmatrix_trans(pack_f16(p0, p1));
+  const uint32_t pb1 = movmatrix_trans(pack_f16(p2, p3));
 
-  // V rows ra, rb (low / high half of b0) and 8 + ra, 8 + rb (of b1); this
-  // lane's 4 bytes of dim group u are dims 32u + 4 gr .. + 3
-  const uint32_t va = vt + ra * D + ((4u * gr) ^ fp8_row_swz<D>(ra));
-  const uint32_t vb = vt + rb * D + ((4u * gr) ^ fp8_row_swz<D>(rb));
-  const uint32_t vc = vt + (8 + ra) * D + ((4u * gr) ^ fp8_row_swz<D>(8 + ra));
-  const uint32_t vd = vt + (8 + rb) * D + ((4u * gr) ^ fp8_row_swz<D>(8 + rb));
-  // edge pages zero the V rows of masked keys (P = 0 times a NaN code is NaN);
-  // the others skip the masking
+  // O^T += V^T P^T. A registers of tile 4u + t: rows (ra, rb) of dim
+  // 64u + 8 gr + t, the same rows of dim + 4, then rows (8 + ra, 8 + rb) of
+  // both dims. Edge pages zero the V values of masked keys (P = 0 times a NaN
+  // code is NaN); the others skip the masking.
   auto pv = [&](auto masked) {
+    auto mk = [&](uint32_t h, uint32_t msk) { return decltype(masked)::value ? h & msk : h; };
 #pragma unroll
-    for (int u = 0; u < D / 32; ++u) {
-      // 32u sets bits 5-6 of the in-row offset, which the swizzle XORs: apply
-      // the group's offset with XOR as well (4 gr only occupies bits 2-4)
-      const uint32_t wa = lds_u32(va ^ (32u * u)), wb = lds_u32(vb ^ (32u * u));
-      const uint32_t wc = lds_u32(vc ^ (32u * u)), wd = lds_u32(vd ^ (32u * u));
-      const uint32_t p01 = __byte_perm(wa, wb, 0x5140), p23 = __byte_perm(wa, wb, 0x7362);
-      const uint32_t q01 = __byte_perm(wc, wd, 0x5140), q23 = __byte_perm(wc, wd, 0x7362);
-      auto lo = [&](uint32_t w, uint32_t m) {
-        const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(w));
-        return decltype(masked)::value ? h & m : h;
-      };
-      auto hi = [&](uint32_t w, uint32_t m) {
-        const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
-        return decltype(masked)::value ? h & m : h;
-      };
-      mma_f16_16816(acc[4 * u + 0], pa, lo(p01, mlo), lo(q01, mhi));
-      mma_f16_16816(acc[4 * u + 1], pa, hi(p01, mlo), hi(q01, mhi));
-      mma_f16_16816(acc[4 * u + 2], pa, lo(p23, mlo), lo(q23, mhi));
-      mma_f16_16816(acc[4 * u + 3], pa, hi(p23, mlo), hi(q23, mhi));
+    for (int u = 0; u < D / 64; ++u) {
+      const uint32_t x01 = __byte_perm(vw[u][0][0], vw[u][1][0], 0x5140);
+      const uint32_t x23 = __byte_perm(vw[u][0][0], vw[u][1][0], 0x7362);
+      const uint32_t y01 = __byte_perm(vw[u][0][1], vw[u][1][1], 0x5140);
+      const uint32_t y23 = __byte_perm(vw[u][0][1], vw[u][1][1], 0x7362);
+      const uint32_t z01 = __byte_perm(vw[u][2][0], vw[u][3][0], 0x5140);
+      const uint32_t z23 = __byte_perm(vw[u][2][0], vw[u][3][0], 0x7362);
+      const uint32_t w01 = __byte_perm(vw[u][2][1], vw[u][3][1], 0x5140);
+      const uint32_t w23 = __byte_perm(vw[u][2][1], vw[u][3][1], 0x7362);
+      const uint32_t a0[4] = {mk(e4m3_lo(x01), mlo), mk(e4m3_lo(y01), mlo),
+                              mk(e4m3_lo(z01), mhi), mk(e4m3_lo(w01), mhi)};
+      mma_f16_16816(acc[4 * u + 0], a0, pb0, pb1);
+      const uint32_t a1[4] = {mk(e4m3_hi(x01), mlo), mk(e4m3_hi(y01), mlo),
+                              mk(e4m3_hi(z01), mhi), mk(e4m3_hi(w01), mhi)};
+      mma_f16_16816(acc[4 * u + 1], a1, pb0, pb1);
+      const uint32_t a2[4] = {mk(e4m3_lo(x23), mlo), mk(e4m3_lo(y23), mlo),
+                              mk(e4m3_lo(z23), mhi), mk(e4m3_lo(w23), mhi)};
+      mma_f16_16816(acc[4 * u + 2], a2, pb0, pb1);
+      const uint32_t a3[4] = {mk(e4m3_hi(x23), mlo), mk(e4m3_hi(y23), mlo),
+                              mk(e4m3_hi(z23), mhi), mk(e4m3_hi(w23), mhi)};
+      mma_f16_16816(acc[4 * u + 3], a3, pb0, pb1);
     }
   };
   if (edge)
@@ -504,7 +537,7 @@ __device__ __forceinline__ void consume_page_fp8(const uint32_t (&qa)[D / 16][4]
 }
 
 template <int D>
-__global__ void __launch_bounds__((kMaxConsumerWarps<D> + 1) * 32, 1)
+__global__ void __launch_bounds__((kFp8ConsumerWarps + 1) * 32, 2)
 decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const DecodeArgs a,
                   const float* __restrict__ k_scale, const float* __restrict__ v_scale,
@@ -600,20 +633,19 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
   // -------------------------------------------------------------- consumers
   const int g = warp / mt, mti = warp % mt;
   const int kvh = hc * hg + g;
-  const int qh0 = kvh * G + mti * 16;
-  const int nrows = min(16, G - mti * 16);
+  const int qh0 = kvh * G + mti * 8;  // the warp's heads: columns 0 .. nh - 1
+  const int nh = min(8, G - mti * 8);
   const int gr = lane >> 2, tq = lane & 3;
   const float sl2 = a.scale_log2 * k_scale[kvh];
   const float vsc = v_scale[kvh];
 
-  // query fragments, rounded to fp16, in the dim order of the K reads: k-step
-  // 4 qc + j takes dims 64 qc + 16 tq + 4 j + {0, 1} (k = 2 tq, 2 tq + 1) and
-  // + {2, 3} (k = 2 tq + 8, 2 tq + 9)
-  uint32_t qa[D / 16][4];
+  // query of head gr (the B operand's column), rounded to fp16, in the dim
+  // order of the K reads: k-step 4 qc + j takes dims 64 qc + 16 tq + 4 j +
+  // {0, 1} (k = 2 tq, 2 tq + 1) and + {2, 3} (k = 2 tq + 8, 2 tq + 9)
+  uint32_t qb[D / 16][2];
   {
     const uint32_t* q32 = static_cast<const uint32_t*>(a.q);
-    const int64_t ra = (static_cast<int64_t>(b) * a.Hq + qh0 + gr) * (D / 2);
-    const int64_t rb = ra + 8 * (D / 2);
+    const int64_t rq = (static_cast<int64_t>(b) * a.Hq + qh0 + gr) * (D / 2);
     auto h2 = [](uint32_t w) {
       return pack_f16(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
     };
@@ -622,17 +654,15 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int w = 32 * qc + 8 * tq + 2 * j;  // word w holds dims 2w, 2w + 1
-        qa[4 * qc + j][0] = gr < nrows ? h2(q32[ra + w]) : 0u;
-        qa[4 * qc + j][1] = gr + 8 < nrows ? h2(q32[rb + w]) : 0u;
-        qa[4 * qc + j][2] = gr < nrows ? h2(q32[ra + w + 1]) : 0u;
-        qa[4 * qc + j][3] = gr + 8 < nrows ? h2(q32[rb + w + 1]) : 0u;
+        qb[4 * qc + j][0] = gr < nh ? h2(q32[rq + w]) : 0u;
+        qb[4 * qc + j][1] = gr < nh ? h2(q32[rq + w + 1]) : 0u;
       }
   }
 
-  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;
-  float acc[D / 8][4];
+  float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+  float acc[D / 16][4];
 #pragma unroll
-  for (int j = 0; j < D / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+  for (int t = 0; t < D / 16; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
   for (int i = 0; i < npg; ++i) {
     const int st = i % ns;
@@ -645,50 +675,49 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap kmap,
     const int phys = phys_s[st];
     if (phys >= 0) {
       const uint32_t kt = base + st * stage_bytes + static_cast<uint32_t>(g * kBlk * D);
-      consume_page_fp8<D>(qa, kt, kt + stage_bytes / 2, (pstart + i) * kBlk, r, sl2, gr, tq, m0,
-                          m1, l0, l1, acc);
+      consume_page_fp8<D>(qb, kt, kt + stage_bytes / 2, (pstart + i) * kBlk, r, sl2, gr, tq, m,
+                          l, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty(st));
   }
 
   // ------------------------------------------------------------- epilogue
-  // dim 32u + 8 tq + t of a row is acc[4u + t][2 half], dim 32u + 8 tq + 4 + t
-  // is acc[4u + t][2 half + 1]: 8 consecutive dims per lane and group
-  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
-  l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
-  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
-  l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+  // head 2 tq + i: dim 64u + 8 gr + t is acc[4u + t][i], dim 64u + 8 gr + 4 + t
+  // is acc[4u + t][2 + i]: 8 consecutive dims per lane, head and group
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int row = gr + 8 * half;
-    if (row >= nrows) continue;
-    const int h = qh0 + row;
-    const float l = half ? l1 : l0;
-    const float m = half ? m1 : m0;
-    const float inv = l > 0.f ? vsc / l : 0.f;
-    const float lse_v = l > 0.f ? (m + log2f(l)) * kLn2 : kNegInf;
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) l[i] += __shfl_xor_sync(0xFFFFFFFFu, l[i], o);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int n = 2 * tq + i;
+    if (n >= nh) continue;
+    const int h = qh0 + n;
+    const float inv = l[i] > 0.f ? vsc / l[i] : 0.f;
+    const float lse_v = l[i] > 0.f ? (m[i] + log2f(l[i])) * kLn2 : kNegInf;
     const int64_t bh = static_cast<int64_t>(b) * a.Hq + h;
-    const int e0 = 2 * half, e1 = 2 * half + 1;
     if (single) {
       uint4* o4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) + bh * D);
 #pragma unroll
-      for (int u = 0; u < D / 32; ++u)
-        o4[4 * u + tq] = make_uint4(pack_bf16(acc[4 * u][e0] * inv, acc[4 * u + 1][e0] * inv),
-                                    pack_bf16(acc[4 * u + 2][e0] * inv, acc[4 * u + 3][e0] * inv),
-                                    pack_bf16(acc[4 * u][e1] * inv, acc[4 * u + 1][e1] * inv),
-                                    pack_bf16(acc[4 * u + 2][e1] * inv, acc[4 * u + 3][e1] * inv));
-      if (tq == 0 && a.lse) a.lse[h * a.B + b] = lse_v;
+      for (int u = 0; u < D / 64; ++u)
+        o4[8 * u + gr] =
+            make_uint4(pack_bf16(acc[4 * u][i] * inv, acc[4 * u + 1][i] * inv),
+                       pack_bf16(acc[4 * u + 2][i] * inv, acc[4 * u + 3][i] * inv),
+                       pack_bf16(acc[4 * u][2 + i] * inv, acc[4 * u + 1][2 + i] * inv),
+                       pack_bf16(acc[4 * u + 2][2 + i] * inv, acc[4 * u + 3][2 + i] * inv));
+      if (gr == 0 && a.lse) a.lse[h * a.B + b] = lse_v;
     } else {
       float4* w = reinterpret_cast<float4*>(a.ws_o + (bh * num_splits + s) * D);
 #pragma unroll
-      for (int u = 0; u < D / 32; ++u) {
-        w[8 * u + 2 * tq] = make_float4(acc[4 * u][e0] * inv, acc[4 * u + 1][e0] * inv,
-                                        acc[4 * u + 2][e0] * inv, acc[4 * u + 3][e0] * inv);
-        w[8 * u + 2 * tq + 1] = make_float4(acc[4 * u][e1] * inv, acc[4 * u + 1][e1] * inv,
-                                            acc[4 * u + 2][e1] * inv, acc[4 * u + 3][e1] * inv);
+      for (int u = 0; u < D / 64; ++u) {
+        w[16 * u + 2 * gr] = make_float4(acc[4 * u][i] * inv, acc[4 * u + 1][i] * inv,
+                                         acc[4 * u + 2][i] * inv, acc[4 * u + 3][i] * inv);
+        w[16 * u + 2 * gr + 1] =
+            make_float4(acc[4 * u][2 + i] * inv, acc[4 * u + 1][2 + i] * inv,
+                        acc[4 * u + 2][2 + i] * inv, acc[4 * u + 3][2 + i] * inv);
       }
-      if (tq == 0) a.ws_lse[bh * num_splits + s] = lse_v;
+      if (gr == 0) a.ws_lse[bh * num_splits + s] = lse_v;
     }
   }
 }
@@ -917,16 +946,20 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_
     p.threads = 128;
   } else {
     const int P = d / 64;
-    const int max_warps = d == 128 ? kMaxConsumerWarps<128> : kMaxConsumerWarps<64>;
-    p.mt = (G + 15) / 16;
+    // a bf16 consumer warp serves 16 query heads (MMA rows), an FP8 one 8
+    // (MMA columns of the transposed products)
+    const int max_warps =
+        fp8 ? kFp8ConsumerWarps : (d == 128 ? kMaxConsumerWarps<128> : kMaxConsumerWarps<64>);
+    p.mt = fp8 ? (G + 7) / 8 : (G + 15) / 16;
     int hg = 1;
     for (int c = 1; c <= Hkv; ++c)
       if (Hkv % c == 0 && c * p.mt <= max_warps && 2 * c * P * kBox <= 64 * 1024) hg = c;
     p.hg = hg;
     p.head_chunks = Hkv / hg;
-    // FP8 pages are half the bytes
+    // FP8 pages are half the bytes, and two FP8 CTAs share an SM (its
+    // registers allow it), each with half the ring
     const int stage = fp8 ? hg * P * kBox : 2 * hg * P * kBox;
-    int ns = 200 * 1024 / stage;
+    int ns = (fp8 ? 100 : 200) * 1024 / stage;
     p.stages = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
     p.threads = (hg * p.mt + 1) * 32;
   }

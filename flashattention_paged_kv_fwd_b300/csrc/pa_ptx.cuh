@@ -347,12 +347,22 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Transpose of an 8x8 matrix of 16-bit values held one row pair per lane
+// (lane l: row l / 4, columns 2 (l % 4), +1), returned in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
 // Shared-memory loads at a 32-bit shared address (volatile: they stay after
 // the mbarrier wait that made the bytes visible).
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t r;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(addr));
   return r;
+}
+__device__ __forceinline__ void lds_v2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 __device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
