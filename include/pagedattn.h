@@ -361,7 +361,10 @@ PA_API size_t pa_decode_workspace_bytes(int B, int Hq, int Hkv, int d, int max_b
  *    element, pools [num_blocks, block_size, Hkv, d] of uint8 like the bf16
  *    pools;
  *  - scales: k_scale[Hkv] and v_scale[Hkv], float32 device arrays; a code q of
- *    KV head h stands for value(q) * scale[h].
+ *    KV head h stands for value(q) * scale[h]. Scales must be finite and > 0:
+ *    they live on the device, so the host cannot check them, and the decode
+ *    folds the key scale into the softmax scale (a scale <= 0 would turn the
+ *    running max into a running min: the result is then unspecified).
  */
 
 /*
@@ -382,10 +385,11 @@ PA_API int pa_kv_append_paged_fp8(const void* k_new, const void* v_new, void* k_
 /*
  * attn_decode_paged_fp8 -- attn_decode_paged over FP8 pools: the attention of
  * each query over the dequantised keys and values value(q) * scale[h]. q and o
- * are bf16; the keys and values are converted exactly to fp16 on chip and the
+ * are bf16; the keys and values are converted exactly to fp16 on chip, the
  * query is rounded to fp16 (exact for bf16 values of magnitude 2^-14 .. 65504)
- * for the warp MMAs; the key scale is folded into the head's softmax scale and
- * the value scale into its output; fp32 accumulation. Arguments, workspace
+ * and the probabilities to fp16 for the warp MMAs; the key scale is folded
+ * into the head's softmax scale and the value scale into its output; fp32
+ * accumulation. Arguments, workspace
  * (size it with pa_decode_workspace_bytes) and errors as attn_decode_paged;
  * block_size must be 16. Alignment: q, o, pools 16 bytes; workspace 256.
  */
