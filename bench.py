@@ -36,7 +36,6 @@ times each of them after the mixed step, under ``workloads``.
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess

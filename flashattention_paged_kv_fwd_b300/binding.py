@@ -8,7 +8,6 @@ If the shared library is missing the first call raises ``RuntimeError``.
 """
 
 import ctypes
-import math
 import os
 
 import torch
@@ -539,10 +538,6 @@ def attn_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, se
                                       _ptr(err_flag), _stream(stream))
     _check(st, "attn_decode_paged_fp8")
     return out, lse
-
-
-def default_scale(head_dim):
-    return 1.0 / math.sqrt(head_dim)
 
 
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

@@ -1,7 +1,6 @@
 """attn_decode_paged on the GPU vs the oracle (naive block-table walk + full
 softmax in fp64)."""
 
-import math
 
 import numpy as np
 import pytest
