@@ -180,19 +180,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 
 // 16-lane shapes: a warp reaches 16 lanes (base lane + 0..15 of its quarter)
 // and four threads share a lane. .16x256b with 8 repetitions covers 64
@@ -211,19 +198,6 @@ __device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, uint32_t (&r)[3
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st16x256_x8(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x256b.x8.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-          taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
 }
 // .16x256b with 4 repetitions: 32 columns, the same mapping as above.
 __device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
@@ -356,11 +330,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 // Shared-memory loads at a 32-bit shared address (volatile: they stay after
 // the mbarrier wait that made the bytes visible).
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t r;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(addr));
-  return r;
-}
 __device__ __forceinline__ void lds_v2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
@@ -435,33 +404,6 @@ __device__ __forceinline__ void umma_ss_k128_elect(uint32_t d, uint64_t a, uint6
       "add.s64 a1, %1, 1028;\n\tadd.s64 b1, %2, 1028;\n\t"
       "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
       "add.s64 a1, %1, 1030;\n\tadd.s64 b1, %2, 1030;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
-      "}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc)
-      : "memory");
-}
-// S = Q K^T for d = 128 with a 64-key K tile: eight 16-wide k-steps; Q's
-// second 64-column panel is 16 KB further (1024 descriptor units), the K
-// tile's (64 rows x 128 bytes) 8 KB further (512 units).
-__device__ __forceinline__ void umma_ss_k128_bn64_elect(uint32_t d, uint64_t a, uint64_t b,
-                                                        uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t.reg .b64 a1, b1;\n\t"
-      "elect.sync _|P, 0xffffffff;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;\n\t"
-      "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
-      "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
-      "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
-      "add.s64 a1, %1, 1024;\n\tadd.s64 b1, %2, 512;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
-      "add.s64 a1, %1, 1026;\n\tadd.s64 b1, %2, 514;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
-      "add.s64 a1, %1, 1028;\n\tadd.s64 b1, %2, 516;\n\t"
-      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
-      "add.s64 a1, %1, 1030;\n\tadd.s64 b1, %2, 518;\n\t"
       "@P tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
       "}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc)
