@@ -89,6 +89,19 @@ def test_decode_f32(lengths, hq, hkv, d, num_splits):
     assert_close(lse.cpu(), want_lse, "lse", F32_MAX)
 
 
+@pytest.mark.parametrize("num_splits", [0, 255])
+def test_decode_one_long_sequence_many_ranges(num_splits):
+    """One sequence of 131 071 keys (8192 blocks, the last one ragged) with the
+    Llama-3-70B grouping: the automatic plan cuts it into about one range per
+    SM and num_splits=255 into 249 ranges of 33 blocks, so the merge combines
+    well over a hundred partials per head; every head is compared with the
+    oracle."""
+    o, lse, want_o, want_lse = run_case([131071], 64, 8, 128, torch.bfloat16,
+                                        num_splits=num_splits, seed=91)
+    assert_close_bf16(o, want_o, "o")
+    assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
+
+
 def test_decode_reports_bad_block():
     lengths = [40, 40]
     w = inputs.make_paged_cache(lengths, lengths, 2, 64, torch.bfloat16, 3, "cuda")

@@ -126,6 +126,30 @@ def test_prefill_rescale_within_and_across_tiles(hq, hkv, window):
     assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
 
 
+@pytest.mark.parametrize("window", [0, 4096])
+def test_prefill_one_long_sequence_sampled(window):
+    """One causal sequence of 32 845 tokens (257 query tiles, the last one
+    ragged; Hq=8, Hkv=2, d=128): the work list spans 257 levels and the
+    longest units stream 257 key tiles. Rows at tile edges, both ends and at
+    random, for heads of both KV groups, against the oracle one row at a time."""
+    n = 32 * 1024 + 77
+    w = inputs.make_prefill([n], 8, 2, 128, torch.bfloat16, 321 + window, "cuda")
+    err = binding.new_err_flag()
+    o, lse = binding.attn_prefill(w["q"], w["k"], w["v"], causal=True, window=window,
+                                  cu_seqlens=w["cu_seqlens"], max_seqlen=n, err_flag=err)
+    binding.check_err_flag(err)
+    rng = np.random.default_rng(window)
+    picks = [0, 1, 127, 128, 4095, 4096, 4097, 16383, n - 78, n - 77, n - 2, n - 1]
+    picks += [int(x) for x in rng.integers(0, n, 8)]
+    rows = [(i, h) for i in picks for h in (0, 3, 4, 7)]
+    want_o, want_lse = oracle.sdpa_rows(w["q"].cpu(), w["k"].cpu(), w["v"].cpu(), rows,
+                                        causal=True, window=window)
+    got_o = torch.stack([o[i, h] for i, h in rows])
+    got_lse = torch.stack([lse[h, i] for i, h in rows])
+    assert_close_bf16(got_o, want_o, "o")
+    assert_close(got_lse.cpu(), want_lse, "lse", LSE_TOL)
+
+
 @pytest.mark.parametrize("hq,hkv,d", [(4, 2, 64), (8, 8, 128)])
 @pytest.mark.parametrize("window", [0, 33])
 def test_prefill_f32(hq, hkv, d, window):
