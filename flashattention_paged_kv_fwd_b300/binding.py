@@ -17,9 +17,19 @@ __all__ = [
     "library_path",
     "load_library",
     "attn_prefill",
+    "attn_prefill_paged",
+    "attn_prefill_backward",
+    "prefill_backward_workspace_bytes",
     "kv_append_paged",
+    "kv_append_paged_fp8",
     "attn_decode_paged",
+    "attn_decode_paged_fp8",
+    "attn_decode_paged_noalloc",
     "decode_workspace_bytes",
+    "copy_blocks",
+    "mla_decode_paged",
+    "mla_append_paged",
+    "mla_decode_workspace_bytes",
     "check_err_flag",
     "new_err_flag",
     "PA_BF16",

@@ -37,8 +37,27 @@ def test_header_declares_the_entry_points():
                  "pa_copy_blocks", "pa_attn_decode_paged", "pa_decode_workspace_bytes",
                  "pa_attn_prefill_backward", "pa_attn_prefill_backward_workspace_bytes",
                  "pa_mla_decode_paged", "pa_mla_decode_workspace_bytes", "pa_mla_append_paged",
-                 "pa_status_str", "pa_attn_decode_paged_noalloc", "pa_testing_set_wait_limit_ns"):
+                 "pa_status_str", "pa_attn_decode_paged_noalloc", "pa_testing_set_wait_limit_ns",
+                 "pa_kv_append_paged_fp8", "pa_attn_decode_paged_fp8"):
         assert name in syms
+
+
+def test_binding_wraps_every_entry_point():
+    """Each entry point of the operation's header has a same-named binding
+    function (without the pa_ prefix) listed in binding.__all__; the status
+    strings are used inside the binding and the testing hooks are not part of
+    the operation."""
+    text = open(os.path.join(ROOT, "include", "pagedattn.h")).read()
+    names = sorted(set(re.findall(r"PA_API[^;(]*?\b(pa_\w+)\s*\(", text)))
+    rename = {"attn_prefill_backward_workspace_bytes": "prefill_backward_workspace_bytes"}
+    for name in names:
+        if name == "pa_status_str":
+            continue
+        py = rename.get(name[3:], name[3:])
+        assert py in binding.__all__, name
+        assert callable(getattr(binding, py)), name
+    for py in binding.__all__:
+        assert hasattr(binding, py), py
 
 
 def test_library_exports_every_declared_symbol(lib):
