@@ -214,7 +214,7 @@ int pa_attn_decode_paged(const void* q, const void* k_cache, const void* v_cache
   const bool f32 = dtype == PA_F32;
   // bf16: the G query heads of a KV head are packed 16 per warp, at most
   // 8 (d = 128) or 12 (d = 64) warps per KV head.
-  if (!f32 && (Hq / Hkv + 15) / 16 > (d == 128 ? 8 : 12)) return PA_ERR_UNSUPPORTED;
+  if (!f32 && Hq / Hkv > pa::decode_max_group(d, false)) return PA_ERR_UNSUPPORTED;
   const pa::DecodePlan p = pa::plan_decode(B, Hq, Hkv, d, max_blocks_per_seq, block_size, window,
                                            num_splits, num_splits > 0 ? 0 : sm_count(), f32);
   if (p.workspace > 0 && (!workspace || workspace_bytes < p.workspace)) return PA_ERR_WORKSPACE;
@@ -292,7 +292,7 @@ int pa_attn_decode_paged_fp8(const void* q, const void* k_cache, const void* v_c
       !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (err_flag && !aligned(err_flag, 4)))
     return PA_ERR_INVALID_ARG;
   if (workspace && !aligned(workspace, 256)) return PA_ERR_INVALID_ARG;
-  if ((Hq / Hkv + 15) / 16 > (d == 128 ? 8 : 12)) return PA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > pa::decode_max_group(d, true)) return PA_ERR_UNSUPPORTED;
   const pa::DecodePlan p = pa::plan_decode(B, Hq, Hkv, d, max_blocks_per_seq, block_size, window,
                                            num_splits, num_splits > 0 ? 0 : sm_count(), false,
                                            true);

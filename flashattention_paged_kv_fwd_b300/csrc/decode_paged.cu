@@ -927,6 +927,11 @@ void ensure_smem_attr_fp8(size_t bytes) {
 
 }  // namespace
 
+int decode_max_group(int d, bool fp8) {
+  if (fp8) return 8 * kFp8ConsumerWarps;
+  return 16 * (d == 128 ? kMaxConsumerWarps<128> : kMaxConsumerWarps<64>);
+}
+
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_size, int window,
                        int num_splits_req, int sm_count, bool f32, bool fp8) {
   DecodePlan p{};

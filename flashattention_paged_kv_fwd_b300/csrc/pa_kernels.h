@@ -45,6 +45,11 @@ struct DecodePlan {
 DecodePlan plan_decode(int B, int Hq, int Hkv, int d, int max_blocks, int block_size, int window,
                        int num_splits_req, int sm_count, bool f32, bool fp8 = false);
 
+// Largest Hq / Hkv the bf16 (or FP8) decode kernel serves: its consumer warps
+// per CTA times the query heads one warp takes (16 as MMA rows for bf16, 8 as
+// MMA columns for FP8).
+int decode_max_group(int d, bool fp8);
+
 struct DecodeArgs {
   const void* q;
   void* o;

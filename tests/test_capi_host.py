@@ -268,6 +268,27 @@ def test_decode_host_validation(lib):
     assert _decode(lib, Hq=256, Hkv=1, d=128, ns=1) == PA_ERR_UNSUPPORTED
 
 
+def test_decode_fp8_host_validation(lib):
+    """Calls the FP8 decode must refuse before any CUDA call (the pointers
+    are fake): at most 64 query heads per KV head (8 warps of 8 heads), pages
+    of 16 tokens, scales given."""
+    f = lib.pa_attn_decode_paged_fp8
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                  f32, i32, vp, ctypes.c_size_t, vp, vp]
+    f.restype = i32
+
+    def call(Hq=8, Hkv=1, d=128, bs=16, k_scale=FAKE, ns=1):
+        return f(FAKE, FAKE, FAKE, k_scale, FAKE, FAKE, 8, FAKE, FAKE, None, 2, Hq, Hkv, d, bs,
+                 16, 0, 0.0, ns, None, 0, None, None)
+
+    assert call(Hq=72) == PA_ERR_UNSUPPORTED     # 9 warps of heads for one KV head
+    assert call(Hq=128) == PA_ERR_UNSUPPORTED
+    assert call(bs=8) == PA_ERR_UNSUPPORTED
+    assert call(k_scale=None) == PA_ERR_INVALID_ARG
+    assert call(Hq=6, Hkv=4) == PA_ERR_INVALID_ARG
+
+
 def test_workspace_bytes_explicit_splits(lib):
     f = lib.pa_decode_workspace_bytes
     # B=2, Hq=4, d=64, 8 blocks in 4 ranges of 2: partial o (fp32) + lse, 256-B aligned parts
