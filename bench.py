@@ -647,7 +647,7 @@ def time_workloads(names, args, dev, binding, flush, stream, world, peaks, peak_
 
 
 def pinned_link_gbs(device, nbytes=256 * 1024 * 1024, reps=5):
-    """Host<->device copy bandwidth from pinned memory on this box (best of
+    """Host<->device copy bandwidth from pinned memory on this machine (best of
     `reps`, CUDA events), the bound the end-to-end copies run against."""
     h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     d = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -836,8 +836,8 @@ def run_e2e(st, args, stream, world):
     * pipelined: steps over three streams with two sets of device input and
       output buffers (the inputs of step i+1 and the outputs of step i-1 move
       while step i computes), the throughput. ``value`` is this one.
-    The box's pinned host<->device bandwidth is measured beside them, so the
-    copies' share of a step can be judged against the link."""
+    The machine's pinned host<->device bandwidth is measured beside them, so
+    the copies' share of a step can be compared with the link."""
     w = st.w
     pre = w["prefill"]
     device = w["q_dec"].device
