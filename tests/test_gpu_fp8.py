@@ -86,6 +86,17 @@ def test_decode_fp8(lengths, hq, hkv, d, num_splits):
     assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
 
 
+@pytest.mark.parametrize("num_splits,window", [(0, 0), (255, 0), (0, 4096)])
+def test_decode_fp8_one_long_sequence(num_splits, window):
+    """One sequence of 131 071 keys over an FP8 cache with the Llama-3-70B
+    grouping: many split ranges merged (automatic plan, 249 ranges), and a
+    window that keeps only the last 4096 keys."""
+    o, lse, want_o, want_lse = run_decode([131071], 64, 8, 128, window=window,
+                                          num_splits=num_splits, seed=93 + window)
+    assert_close_bf16(o, want_o, "o")
+    assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
+
+
 @pytest.mark.parametrize("window", [1, 16, 17, 100])
 def test_decode_fp8_window(window):
     o, lse, want_o, want_lse = run_decode([3, 40, 257, 999], 16, 4, 128, window=window,
