@@ -515,7 +515,8 @@ def attn_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, se
                           window=0, scale=None, num_splits=0, out=None, lse=None,
                           return_lse=True, workspace=None, err_flag=None, stream=None):
     """attn_decode_paged over FP8 pools: q bf16 [B, Hq, d]; pools uint8
-    [num_blocks, 16, Hkv, d] of E4M3 codes; k_scale, v_scale float32 [Hkv].
+    [num_blocks, 16, Hkv, d] of E4M3 codes; k_scale, v_scale float32 [Hkv],
+    finite and > 0 (they stay on the device and are not checked).
     Returns (o bf16 [B, Hq, d], lse float32 [Hq, B])."""
     lib = _fp8_fns()
     _cuda_contig("q", q, torch.bfloat16)
