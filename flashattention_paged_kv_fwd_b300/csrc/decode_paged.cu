@@ -413,22 +413,6 @@ __device__ __forceinline__ void consume_page_fp8(const uint32_t (&qb)[D / 16][2]
   const int k0 = fp8_key_row(gr), k1 = 8 + k0;  // this lane's score rows
   const int ra = fp8_key_row(2 * tq), rb = fp8_key_row(2 * tq + 1);  // its V rows (and + 8)
 
-  // V first: the loads do not depend on the scores, so their latency hides
-  // behind S. vw[u][i]: 8 bytes (dims 64u + 8 gr .. + 7) of row ra, rb,
-  // 8 + ra, 8 + rb. 64u sets bit 6 of the in-row offset, 8 gr bits 3-5: the
-  // swizzle XORs bits 4-6 and the row bases keep bit 6 clear, so the group
-  // offset is applied with XOR too.
-  uint32_t vw[D / 64][4][2];
-  {
-    const int rows[4] = {ra, rb, 8 + ra, 8 + rb};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t a = vt + rows[i] * D + ((8u * gr) ^ fp8_row_swz<D>(rows[i]));
-#pragma unroll
-      for (int u = 0; u < D / 64; ++u) lds_v2(a ^ (64u * u), vw[u][i][0], vw[u][i][1]);
-    }
-  }
-
   // S^T, even and odd k-steps in two accumulators (two MMA chains)
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
   {
@@ -451,6 +435,23 @@ __device__ __forceinline__ void consume_page_fp8(const uint32_t (&qb)[D / 16][2]
       }
     }
   }
+  // V once the score MMAs are issued: the loads do not depend on the scores,
+  // so their latency hides behind the MMAs and the softmax, and they hold no
+  // registers across the K reads. vw[u][i]: 8 bytes (dims 64u + 8 gr .. + 7)
+  // of row ra, rb, 8 + ra, 8 + rb. 64u sets bit 6 of the in-row offset, 8 gr
+  // bits 3-5: the swizzle XORs bits 4-6 and the row bases keep bit 6 clear,
+  // so the group offset is applied with XOR too.
+  uint32_t vw[D / 64][4][2];
+  {
+    const int rows[4] = {ra, rb, 8 + ra, 8 + rb};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a = vt + rows[i] * D + ((8u * gr) ^ fp8_row_swz<D>(rows[i]));
+#pragma unroll
+      for (int u = 0; u < D / 64; ++u) lds_v2(a ^ (64u * u), vw[u][i][0], vw[u][i][1]);
+    }
+  }
+
   // sc[0] / sc[1]: row k0, heads 2 tq / 2 tq + 1; sc[2] / sc[3]: row k1
   float sc[4];
 #pragma unroll
