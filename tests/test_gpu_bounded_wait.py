@@ -109,3 +109,37 @@ def test_decode_wait_gives_up_then_next_call_is_correct(wait_limit):
                                            block_size=16)
     assert_close_bf16(o, want_o, "o")
     assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
+
+
+def test_decode_fp8_wait_gives_up_then_next_call_is_correct(wait_limit):
+    lengths = [16000] * 16
+    big = inputs.make_paged_cache_fp8(lengths, lengths, 8, 128, 906, "cuda", poison=False)
+    gen = inputs.make_generator(907, "cuda")
+    qb = inputs.randn((16, 64, 128), torch.bfloat16, gen, "cuda")
+    sl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+
+    def call(err):
+        binding.attn_decode_paged_fp8(qb, big["k_cache"], big["v_cache"], big["k_scale"],
+                                      big["v_scale"], big["block_table"], sl, err_flag=err)
+
+    wait_limit(1)
+    flags = _expire(call)
+    wait_limit(0)
+    assert flags & PA_DEV_TIMEOUT, f"no wait gave up in {ATTEMPTS} calls (flags {flags})"
+    assert flags == PA_DEV_TIMEOUT
+    del big
+    lengths = [1, 40, 257, 1000]
+    w = inputs.make_paged_cache_fp8(lengths, lengths, 2, 128, 908, "cuda", spare_blocks=2)
+    q = inputs.randn((4, 16, 128), torch.bfloat16, gen, "cuda")
+    sl = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    err = binding.new_err_flag()
+    o, lse = binding.attn_decode_paged_fp8(q, w["k_cache"], w["v_cache"], w["k_scale"],
+                                           w["v_scale"], w["block_table"], sl, num_splits=3,
+                                           err_flag=err)
+    binding.check_err_flag(err)
+    want_o, want_lse = oracle.decode_paged_fp8(q.cpu(), w["k_cache"].cpu().numpy(),
+                                               w["v_cache"].cpu().numpy(), w["k_scale"].cpu(),
+                                               w["v_scale"].cpu(), w["block_table"].cpu().tolist(),
+                                               lengths, block_size=16)
+    assert_close_bf16(o, want_o, "o")
+    assert_close(lse.cpu(), want_lse, "lse", LSE_TOL)
