@@ -27,7 +27,11 @@ struct BackwardArgs {
   float scale;       // softmax scale (natural units)
   float scale_log2;  // scale * log2(e)
   int n_units;       // key tiles x KV heads x sequences enumerated by the main kernel
+  unsigned long long wait_ns;  // give-up limit of the pipeline waits (role_wait_limit_ns())
 };
+
+// Give-up limit of the kernels' pipeline waits (2 s unless a test shortened it).
+unsigned long long role_wait_limit_ns();
 
 // Bytes of workspace the backward pass needs for T packed tokens.
 size_t backward_workspace_bytes(long long T, int Hq, int d);

@@ -73,6 +73,7 @@ int pa_attn_prefill_backward(const void* q, const void* k, const void* v, const 
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.N = N; a.T = static_cast<int>(T); a.d = d;
   a.max_seqlen = msl; a.causal = causal ? 1 : 0; a.window = window > 0 ? window : 0;
   a.scale_log2 = scale_log2(scale, d);
+  a.wait_ns = pa::role_wait_limit_ns();
   a.scale = static_cast<float>(softmax_scale(scale, d));
   CUtensorMap qm, km, vm, dom, dqm;
   if (!encode_3d(&qm, q, d, Hq, T, 128) || !encode_3d(&km, k, d, Hkv, T, 128) ||

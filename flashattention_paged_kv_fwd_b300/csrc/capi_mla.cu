@@ -97,6 +97,7 @@ int pa_mla_decode_paged(const void* q, const void* cache, const int32_t* block_t
   }
   a.max_blocks = max_blocks_per_seq; a.num_blocks = num_blocks; a.B = B; a.H = H;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  a.wait_ns = pa::role_wait_limit_ns();
   CUtensorMap cm;
   if (!encode_mla_pool(&cm, cache, num_blocks)) return PA_ERR_CUDA;
   const cudaError_t e = pa::launch_mla_decode_bf16(a, p, cm, static_cast<cudaStream_t>(stream));

@@ -158,7 +158,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap cmap, const MlaArgs a, con
       uint32_t loaded = 0;  // stages whose last fill had copies in flight
       for (int i = 0; i < nsteps; ++i) {
         const int st = i % ns, u = i / ns;
-        if (u > 0 && !mbar_wait(empty(st), (u - 1) & 1)) {
+        if (u > 0 && !mbar_wait(empty(st), (u - 1) & 1, a.wait_ns)) {
           raise_err(a.err, kDevErrTimeout);
           *abort_s = 1;
           break;
@@ -223,7 +223,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap cmap, const MlaArgs a, con
   for (int i = 0; i < nsteps; ++i) {
     const int st = i % ns;
     // warp-uniform: the ldmatrix / mma.sync below need all 32 lanes
-    const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(full(st), (i / ns) & 1));
+    const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(full(st), (i / ns) & 1, a.wait_ns));
     if (!got && lane == 0) {
       raise_err(a.err, kDevErrTimeout);
       *abort_s = 1;
@@ -260,7 +260,7 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap cmap, const MlaArgs a, con
       *reinterpret_cast<float4*>(rb + ((wk * 4 + t) * 32 + lane) * 4) =
           make_float4(sc[t][0], sc[t][1], sc[t][2], sc[t][3]);
     mbar_arrive(xchg(g, buf));
-    const bool synced = mbar_wait(xchg(g, buf), (i >> 1) & 1);
+    const bool synced = mbar_wait(xchg(g, buf), (i >> 1) & 1, a.wait_ns);
     if (!synced && lane == 0) {
       raise_err(a.err, kDevErrTimeout);
       *abort_s = 1;

@@ -42,7 +42,11 @@ struct MlaArgs {
   int32_t* err;
   int max_blocks, num_blocks, B, H;
   float scale_log2;
+  unsigned long long wait_ns;  // give-up limit of the pipeline waits (role_wait_limit_ns())
 };
+
+// Give-up limit of the kernels' pipeline waits (2 s unless a test shortened it).
+unsigned long long role_wait_limit_ns();
 
 // `cmap`: the pool [num_blocks, 16, 576] described as (64 elements, 16
 // tokens, 9 panels, blocks), one 128-byte-swizzled box per block.

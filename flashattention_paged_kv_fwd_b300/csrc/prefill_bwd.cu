@@ -149,16 +149,21 @@ __device__ __forceinline__ int unit_of(int k, int c, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// Bounded wait that also gives up as soon as another role has aborted. The
+// give-up limit sits in shared memory in the word after the abort flag and is
+// read only once the first poll has failed. Short limits (set only by tests
+// of the give-up path) poll without suspending, as mbar_wait does.
 __device__ __forceinline__ bool bw_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t limit_ns = static_cast<uint32_t>(abort_flag[1]);
+  const bool quick = limit_ns < kQuickPollBelowNs;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < (quick ? 4 : 64); ++i)
+      if (mbar_poll(bar, parity, quick)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       return false;
     }
@@ -296,6 +301,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
       mbar_init(bar(C::B_ACCFREE), 256);
       mbar_init(bar(C::B_DRAIN), 1);
       *abort_flag = 0;
+      abort_flag[1] = static_cast<int>(a.wait_ns);  // <= 2 s: fits in 32 bits
       fence_mbar_init();
     }
     __syncwarp();

@@ -2,9 +2,9 @@
  * pagedattn_testing.h -- a hook of libpagedattn.so for tests of its failure
  * handling. Not part of the attention API: the pages have no counterpart.
  *
- * Every wait inside the prefill and decode kernels is bounded. When one role
- * of a kernel (the copy producer, the MMA issuer, the softmax warps, the
- * decode consumers) waits longer than the limit for another, it gives up,
+ * Every wait inside the library's kernels is bounded. When one role of a
+ * kernel (a copy producer, the MMA issuer, the softmax or gradient warps,
+ * the decode consumers) waits longer than the limit for another, it gives up,
  * ORs PA_DEV_TIMEOUT into err_flag, tells the other roles to give up too,
  * waits (with their own limit) for the copies and MMAs it already started,
  * frees what it holds and returns; the outputs of that call are then
@@ -25,9 +25,10 @@ extern "C" {
 
 /*
  * Sets the give-up limit, in nanoseconds, of the waits between the roles of
- * the kernels that pa_attn_prefill, pa_attn_prefill_paged and
- * pa_attn_decode_paged (and its no-allocation variant) launch from now on in
- * this process, and returns the previous limit. 0, or anything above the
+ * the kernels that pa_attn_prefill, pa_attn_prefill_paged,
+ * pa_attn_prefill_backward, pa_attn_decode_paged (and its no-allocation
+ * variant), pa_attn_decode_paged_fp8 and pa_mla_decode_paged launch from now
+ * on in this process, and returns the previous limit. 0, or anything above the
  * default of 2 s, restores the default. Under a limit below 1 ms the waits
  * poll without suspending the waiting threads and read the clock every few
  * polls, so that the limit is seen soon after it runs out. The waits for copies and
