@@ -330,8 +330,9 @@ PA_API int pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_block
  *             count; > 0: the maximum number of ranges per sequence
  *  workspace  device scratch of at least pa_decode_workspace_bytes(...)
  *             bytes for the same arguments (may be NULL when that is 0)
- * block_size must be 16. Alignment: q, o, pools 16-byte aligned; workspace
- * 256-byte aligned.
+ * block_size must be 16, and for bf16 Hq / Hkv at most 128 (d = 128) or 192
+ * (d = 64); otherwise PA_ERR_UNSUPPORTED. Alignment: q, o, pools 16-byte
+ * aligned; workspace 256-byte aligned.
  */
 PA_API int pa_attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* block_table, int max_blocks_per_seq,
@@ -391,7 +392,8 @@ PA_API int pa_kv_append_paged_fp8(const void* k_new, const void* v_new, void* k_
  * into the head's softmax scale and the value scale into its output; fp32
  * accumulation. Arguments, workspace
  * (size it with pa_decode_workspace_bytes) and errors as attn_decode_paged;
- * block_size must be 16. Alignment: q, o, pools 16 bytes; workspace 256.
+ * block_size must be 16 and Hq / Hkv at most 64 (PA_ERR_UNSUPPORTED
+ * otherwise). Alignment: q, o, pools 16 bytes; workspace 256.
  */
 PA_API int pa_attn_decode_paged_fp8(const void* q, const void* k_cache, const void* v_cache,
                                     const float* k_scale, const float* v_scale,
