@@ -48,6 +48,38 @@ def test_append_fp8_bit_exact(hkv, d):
     assert int(kc.cpu().numpy().max()) <= 0xFF
 
 
+@pytest.mark.parametrize("n_seq", [2, 5000])
+def test_append_fp8_flags_tokens_outside_cu_new(n_seq):
+    """cu_new that disagrees with the token count: tokens outside
+    [cu_new[0], cu_new[B]) belong to no sequence, are reported as a bad
+    position and are not written; the others land as the oracle puts them
+    (5000 sequences: the offsets are read from global memory)."""
+    before = [3, 20] + [0] * (n_seq - 2)
+    new = [3, 3] + [0] * (n_seq - 2)
+    c = inputs.make_paged_cache_fp8([b + n for b, n in zip(before, new)], before, 2, 64, 43,
+                                    "cuda", spare_blocks=2)
+    gen = inputs.make_generator(44, "cuda")
+    k_new = inputs.randn((10, 2, 64), torch.bfloat16, gen, "cuda")
+    v_new = inputs.randn((10, 2, 64), torch.bfloat16, gen, "cuda")
+    cu = [2, 5] + [8] * (n_seq - 1)  # tokens 0-1 and 8-9 lie outside every range
+    seq_lens = torch.tensor(before, dtype=torch.int32, device="cuda")
+    cu_new = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    kc, vc = c["k_cache"].clone(), c["v_cache"].clone()
+    err = binding.new_err_flag()
+    binding.kv_append_paged_fp8(k_new, v_new, kc, vc, c["k_scale"], c["v_scale"],
+                                c["block_table"], seq_lens, cu_new=cu_new, err_flag=err)
+    with pytest.raises(binding.PagedAttnError, match="position"):
+        binding.check_err_flag(err)
+    want_k, want_v = oracle.append_paged_fp8(c["k_cache"].cpu().numpy(),
+                                             c["v_cache"].cpu().numpy(), k_new[2:8].cpu(),
+                                             v_new[2:8].cpu(), c["k_scale"].cpu(),
+                                             c["v_scale"].cpu(),
+                                             c["block_table"][:2].cpu().tolist(), before[:2],
+                                             [0, 3, 6], 16)
+    assert np.array_equal(kc.cpu().numpy(), want_k)
+    assert np.array_equal(vc.cpu().numpy(), want_v)
+
+
 def run_decode(lengths, hq, hkv, d, window=0, num_splits=0, seed=0):
     w = inputs.make_paged_cache_fp8(lengths, lengths, hkv, d, seed, "cuda", spare_blocks=2)
     gen = inputs.make_generator(seed + 100, "cuda")
