@@ -35,6 +35,7 @@ CASES = [
     ([64, 129, 700], 8, 1, 64),                      # MQA
     ([5, 500, 999, 31], 64, 8, 128),                 # GQA 8 (Llama-3-70B grouping)
     ([2, 300], 32, 1, 128),                          # G = 32: two 16-row tiles per KV head
+    ([33, 500], 32, 2, 64),                          # G = 16 at d = 64
     ([0, 3, 0, 77], 4, 2, 64),                       # empty sequences
 ]
 

@@ -103,6 +103,7 @@ CASES = [
     ([64, 129, 700], 8, 1, 64),                      # MQA
     ([5, 500, 999, 31], 64, 8, 128),                 # GQA 8 (Llama-3-70B grouping)
     ([2, 300], 32, 1, 128),                          # G = 32: four 8-head warps per KV head
+    ([33, 500], 32, 2, 64),                          # G = 16 at d = 64
     ([7, 130, 64], 24, 2, 128),                      # G = 12: the second warp has 4 heads
     ([33, 400], 6, 1, 64),                           # G = 6: two head columns unused
     ([0, 3, 0, 77], 4, 2, 64),                       # empty sequences
